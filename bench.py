@@ -1,0 +1,397 @@
+"""Benchmark of the GB300 routed-expert MoE FFN layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_bf16] [--tokens 64]
+
+One step = one moe_ffn_forward over a batch of T tokens (router + top-8,
+permutation, grouped gate/up with the clamped SwiGLU, grouped down with the
+weighted scatter-add and the shared expert), weights resident in HBM.  Four
+seeded x batches are cycled so the routed experts differ step to step, and
+L2 is flushed (a 512 MB write) before every timed step; only the layer call
+itself sits between the step's CUDA events.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle, the
+plain implementation written from the method's description, on the host
+cores, on a bounded sample of the same workload.
+
+For N > 1 launch with torch.distributed.run: each rank runs its own replica
+on its own GPU (the layer has no exchange step), "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "MoE layer tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+N_BATCHES = 4
+THROTTLE_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+    0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+    0x100: "display_clock_setting"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ inputs
+
+def host_layer(wl):
+    """Seeded inputs on the host: x batches, router, expert stacks."""
+    x_all = synthetic.gen_x(wl, T=wl.T * N_BATCHES)
+    batches = [np.ascontiguousarray(x_all[i * wl.T:(i + 1) * wl.T]) for i in range(N_BATCHES)]
+    w_router, b_router = synthetic.gen_router(wl)
+    experts = synthetic.gen_experts(wl)
+    shared = synthetic.gen_experts(wl, shared=True)
+    return batches, w_router, b_router, experts, shared
+
+
+def expert_bytes(wl):
+    per = 3 * wl.H * wl.I
+    if wl.fmt == "bf16":
+        return per * 2
+    return per // 2 + per // synthetic.INT4_GROUP * 2
+
+
+def algorithmic_bytes(wl, distinct):
+    """Weights of the distinct routed experts hit + the shared expert, router
+    weight and bias, x in, fp32 out."""
+    return ((distinct + 1) * expert_bytes(wl) + wl.E * wl.H * 2 + wl.E * 4
+            + wl.T * wl.H * 2 + wl.T * wl.H * 4)
+
+
+def gateup_bytes(wl, distinct):
+    """Gate/up kernel: gate+up weights of distinct experts + shared, x_perm
+    rows read, h written (two bf16 planes, or one fp16 plane)."""
+    rows = (wl.top_k + 1) * wl.T
+    w = (distinct + 1) * (2 * wl.I * wl.H) * (2 if wl.fmt == "bf16" else 0.5 + 2 / 32)
+    h = rows * wl.I * (4 if wl.fmt == "bf16" else 2)
+    return w + rows * wl.H * 2 + h
+
+
+def flops_per_token(wl):
+    return 2 * wl.E * wl.H + (wl.top_k + 1) * 2 * 3 * wl.H * wl.I
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 5:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    mask = int(parts[4], 16)
+                except ValueError:
+                    continue
+                for bit, name in THROTTLE_BITS.items():
+                    if mask & bit and name != "gpu_idle":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(wl, x, w_router, b_router, experts, shared, budget_s=12.0):
+    """Times the oracle on successive token slices of x until budget_s."""
+    import oracle
+    done, t0 = 0, time.perf_counter()
+    chunk = max(1, min(x.shape[0], 8))
+    while True:
+        xs = np.ascontiguousarray(x[done % x.shape[0]:done % x.shape[0] + chunk])
+        oracle.moe_forward(xs, w_router, b_router, experts, shared, wl.fmt)
+        done += xs.shape[0]
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done, el, oracle.max_threads()
+
+
+# ------------------------------------------------------------------ main
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="decode_bf16", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_of(wl, world):
+    return {"workload": f"{wl.name} T={wl.T} H={wl.H} E={wl.E} top_k={wl.top_k} I={wl.I} "
+                        f"shared I={wl.I_shared} {wl.fmt} weights",
+            "tokens_per_step": wl.T, "weights": wl.fmt,
+            "expert_weight_bytes": wl.E * expert_bytes(wl),
+            "x_batches_cycled": N_BATCHES,
+            "l2": "flushed before every step (512 MB write); weights read per step exceed L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    batches, w_router, b_router, experts, shared = host_layer(wl)
+    per_step = []
+    tokens = 0
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state; warm-up steps are not timed
+    t_all = 0.0
+    cores = 0
+    for s in range(args.steps):
+        x = batches[s % N_BATCHES]
+        n = min(x.shape[0], 8)
+        import oracle
+        t0 = time.perf_counter()
+        oracle.moe_forward(np.ascontiguousarray(x[:n]), w_router, b_router, experts, shared,
+                           wl.fmt)
+        dt = time.perf_counter() - t0
+        per_step.append(dt)
+        tokens += n
+        t_all += dt
+        cores = oracle.max_threads()
+    value = tokens / t_all
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {min(wl.T, 8)} tokens of each step's batch"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl, rank, world, local):
+    import torch
+    import routed_expert_ffn_sigmoid_gb300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    batches, w_router, b_router, experts, shared = host_layer(wl)
+
+    def up16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev) if a.dtype == np.uint8 else up16(a)
+
+    xs = [up16(b) for b in batches]
+    wr, b = up16(w_router), torch.from_numpy(b_router).to(dev)
+    ex = {k: up(v) for k, v in experts.items()}
+    sh = {k: up(v) for k, v in shared.items()}
+    exw = moe.make_weights(ex["gate"], ex["up"], ex["down"], ex.get("gate_scale"),
+                           ex.get("up_scale"), ex.get("down_scale"))
+    shw = moe.make_weights(sh["gate"], sh["up"], sh["down"], sh.get("gate_scale"),
+                           sh.get("up_scale"), sh.get("down_scale"))
+    dims = moe.make_dims(wl.T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # distinct routed experts per batch (from the library's own routing, untimed)
+    distinct = []
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    wts = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device=dev)
+    for x in xs:
+        moe.moe_router_topk(dims, x, wr, b, idx, wts, ws)
+        distinct.append(int(torch.unique(idx).numel()))
+
+    nst = moe.MOE_STAGE_COUNT
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+        for e in evs:
+            e.record(stream)  # materialise the handle
+        se = moe.MoeStageEvents()
+        for i, e in enumerate(evs):
+            se.ev[i] = e.cuda_event
+        return evs, se
+
+    for s in range(args.warmup):
+        moe.moe_ffn_forward(dims, xs[s % N_BATCHES], wr, b, exw, shw, out, ws)
+    torch.cuda.synchronize(dev)
+    st = moe.moe_workspace_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.moe_status_string(st))
+
+    step_events = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.zero_()
+            moe.moe_ffn_forward_timed(dims, xs[s % N_BATCHES], wr, b, exw, shw, out, ws,
+                                      step_events[s][1])
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    st = moe.moe_workspace_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.moe_status_string(st))
+
+    step_ms = [evs[0].elapsed_time(evs[nst]) for evs, _ in step_events]
+    stage_ms = [[evs[i].elapsed_time(evs[i + 1]) for evs, _ in step_events] for i in range(nst)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_total = wl.T * args.steps * world
+    value = tokens_total / (total_ms / 1e3)
+
+    # end to end through the C ABI with host buffers: H2D x, layer, D2H out
+    host_x = [torch.from_numpy(bt.view(np.int16)).pin_memory() for bt in batches]
+    host_out = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+    xdev = torch.empty_like(xs[0])
+    for s in range(args.warmup):
+        xdev.copy_(host_x[s % N_BATCHES], non_blocking=True)
+        moe.moe_ffn_forward(dims, xdev, wr, b, exw, shw, out, ws)
+        host_out.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for s in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        xdev.copy_(host_x[s % N_BATCHES], non_blocking=True)
+        moe.moe_ffn_forward(dims, xdev, wr, b, exw, shw, out, ws)
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_value = wl.T * args.steps * world / (e2e_ms / 1e3)
+
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+    mean_distinct = sum(distinct[s % N_BATCHES] for s in range(args.steps)) / args.steps
+    gu_ms = statistics.mean(stage_ms[2])
+    gu_bytes = statistics.mean(gateup_bytes(wl, distinct[s % N_BATCHES]) for s in range(args.steps))
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    layer_bytes = statistics.mean(algorithmic_bytes(wl, distinct[s % N_BATCHES])
+                                  for s in range(args.steps))
+    layer_gbs = layer_bytes / (ms_per_step / 1e3) / 1e9
+    tflops = flops_per_token(wl) * wl.T / (ms_per_step / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n, el, cores = oracle_sample(wl, batches[0], w_router, b_router, experts, shared,
+                                     args.cpu_budget_s)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of the same workload (slices of 8 tokens of batch 0), "
+                         f"{el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
+                     "int4 weights dequantised to fp16, fp32 accumulate",
+            "data": "synthetic (seeded generator; random-init weights)",
+            "config": config_of(wl, world),
+            "roofline": {"bound": "hbm", "kernel": "gateup_swiglu (tcgen05 grouped gate/up)",
+                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "peak_source": f"{peak_src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": gu_bytes, "mean_launch_ms": gu_ms},
+            "layer": {"algorithmic_GBps": layer_gbs, "hbm_frac": layer_gbs / hbm_peak,
+                      "tflops": tflops, "tc_frac_sustained": tflops / (tc_sust or tc_peak),
+                      "distinct_experts_mean": mean_distinct,
+                      "stage_ms_mean": {n: statistics.mean(v) for n, v in
+                                        zip(moe.STAGE_NAMES, stage_ms)}},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
+            "gpu_launches": 8 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    wl = synthetic.WORKLOADS[args.workload].with_tokens(args.tokens)
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+    else:
+        run_ours(args, wl, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

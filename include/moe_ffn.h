@@ -1,0 +1,210 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) routed-expert MoE FFN layer.
+ *
+ * The layer (GLM-5.3-Flash MoE FFN; "Add GLM-5.3-Flash (glm5next) support
+ * with ROCmFP mix qtypes (105/106)", lucebox PR #1, sections "Architecture"
+ * and "MoE FFN (REAL routed expert execution)"):
+ *
+ *   z[t][e]   = sum_h x[t][h] * Wr[e][h] + b[e]          router logits
+ *   s[t][e]   = sigmoid(z[t][e])                          routing probability
+ *   sel[t]    = the top_k experts by s (ties: lower e)    top-k selection
+ *   w[t][j]   = s[t][sel_j] / sum_j' s[t][sel_j']         weight normalisation
+ *   FFN_e(v)  = Wd_e . (silu(min(Wg_e v, 10)) * clamp(Wu_e v, -10, 10))
+ *   out[t]    = sum_j w[t][j] FFN_{sel_j}(x_t) + FFN_shared(x_t)
+ *
+ * Int4 storage follows the grouped fmt=4 format with offset-binary decode,
+ * value = (nibble - 8) * scale ("feat(glm53): add device-resident HIP backend
+ * for MI350P", colibri PR #1448, section "Key changes").  Top-k is
+ * deterministic: the lower expert index wins a tie (same section).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *   the moe_dims / moe_weights structs themselves, which are host structs
+ *   read during the call.  The library allocates no device memory and keeps
+ *   no per-call state between calls; scratch lives in the caller's
+ *   workspace (see moe_workspace_size).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream).  Argument errors are reported synchronously, before
+ *   anything is launched.  A failed launch returns MOE_ERR_CUDA.
+ * - Device pointers must be 16-byte aligned.
+ * - bf16 / fp16 values are IEEE bit patterns in uint16 storage.
+ * - T == 0 is a no-op: the call returns MOE_OK and reads or writes nothing.
+ * - Shapes: T >= 0 tokens; H hidden size, multiple of 128; E routed experts,
+ *   top_k <= E <= 512; I expert intermediate size, multiple of 64;
+ *   I_shared == I; 1 <= top_k <= 16.  Other shapes return
+ *   MOE_ERR_UNSUPPORTED.  The device must be sm_103 (GB300).
+ * - There is no CPU fallback: without a suitable GPU every call fails.
+ *
+ * Matrix layouts ("nn.Linear", output-major, reduction dim contiguous):
+ *   x        [T][H]    bf16          router weight Wr [E][H] bf16
+ *   b_router [E]       fp32
+ *   bf16 weights: gate, up [E][I][H]; down [E][H][I]; shared: leading dim 1.
+ *   Int4 (fmt MOE_W_INT4_G32): codes uint8 [E][N][K/2] with element 2m of a
+ *   row in the low nibble of byte m and 2m+1 in the high nibble; scales bf16
+ *   [E][N][K/32], one per 32 consecutive reduction elements.  N x K is the
+ *   matrix shape above (gate/up: N=I, K=H; down: N=H, K=I).
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_FFN_ABI_VERSION 1
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, negative size */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape, top_k, format or GPU not supported */
+  MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+  MOE_ERR_TIMEOUT = 5        /* a device-side wait ran out of time (device status) */
+} moe_status;
+
+typedef enum moe_wfmt {
+  MOE_W_BF16 = 0,            /* bf16 weights */
+  MOE_W_INT4_G32 = 1         /* offset-binary Int4, bf16 scale per 32 elements */
+} moe_wfmt;
+
+typedef struct moe_dims {
+  int32_t T, H, E, I, I_shared, top_k;
+  int32_t fmt;               /* moe_wfmt */
+} moe_dims;
+
+typedef struct moe_weights {
+  const void* gate;          /* bf16 [E][I][H] or Int4 codes [E][I][H/2] */
+  const void* up;            /* bf16 [E][I][H] or Int4 codes [E][I][H/2] */
+  const void* down;          /* bf16 [E][H][I] or Int4 codes [E][H][I/2] */
+  const void* gate_scale;    /* bf16 [E][I][H/32]; NULL for bf16 weights */
+  const void* up_scale;      /* bf16 [E][I][H/32]; NULL for bf16 weights */
+  const void* down_scale;    /* bf16 [E][H][I/32]; NULL for bf16 weights */
+} moe_weights;
+
+/* Library ABI version (MOE_FFN_ABI_VERSION). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/*
+ * Bytes of device workspace the calls below need for these dims (0 if the
+ * dims are invalid).  The same workspace may serve every entry point for the
+ * same dims; calls on one workspace must be stream-ordered.  The first 256
+ * bytes hold the device status word (see moe_workspace_status); the caller
+ * zeroes the workspace once before first use.
+ */
+size_t moe_workspace_size(const moe_dims* d);
+
+/*
+ * Router + top-k: logits with fused bias, sigmoid, top_k selection (ties to
+ * the lower expert index; slot j holds the j-th largest score) and
+ * normalisation of the selected scores.
+ *   x          [T][H] bf16         w_router [E][H] bf16      b_router [E] fp32
+ *   topk_idx   [T][top_k] int32    topk_w   [T][top_k] fp32 (rows sum to 1)
+ * Follows "MoE FFN (REAL routed expert execution)": sigmoid routing, top-8
+ * selection, weight normalisation (lucebox PR #1).
+ */
+moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_router,
+                           const float* b_router, int32_t* topk_idx, float* topk_w, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Counting-sort permutation of the (token, slot) pairs by expert, with the
+ * shared expert appended as group E holding every token in order:
+ *   offsets  [E+2] int32: group g owns rows [offsets[g], offsets[g+1]);
+ *            offsets[E] = top_k*T, offsets[E+1] = (top_k+1)*T
+ *   gather   [(top_k+1)*T] int32: token of each row (ascending within a group)
+ *   row_of   [T][top_k] int32: row holding (t, j)
+ *   x_perm   [(top_k+1)*T][H]: x[gather[r]] -- bf16 for MOE_W_BF16, fp16
+ *            (exact conversion of the bf16 input) for MOE_W_INT4_G32.
+ * The grouping that feeds the per-expert matmuls ("ggml_mul_mat_id for
+ * gate/up/down", lucebox PR #1, "MoE FFN" section).
+ */
+moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, const void* x,
+                       int32_t* offsets, int32_t* gather, int32_t* row_of, void* x_perm, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Grouped expert FFN over permuted rows: for row r of group g,
+ *   y_perm[r] = FFN_g(x_perm[r])   (g == E: the shared expert), fp32 [(top_k+1)T][H],
+ * unweighted.  Gate/up and down run on tcgen05 tensor cores with fp32
+ * accumulation; the clamped SwiGLU ("gate (-inf, 10] -> SiLU, up [-10, 10]",
+ * lucebox PR #1, Architecture) is fused into the gate/up epilogue.
+ * x_perm and offsets as produced by moe_permute.
+ */
+moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* offsets,
+                          const moe_weights* experts, const moe_weights* shared, float* y_perm,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Weighted combination in a fixed order ("Weighted combination of expert
+ * outputs", lucebox PR #1, "What Executes vs. TODO" item 3):
+ *   out[t] = sum_{j=0..top_k-1} topk_w[t][j] * y_perm[row_of[t][j]] + y_perm[top_k*T + t]
+ * out fp32 [T][H] is overwritten.  Bitwise reproducible run to run.
+ */
+moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* row_of,
+                       const float* topk_w, float* out, moe_stream_t stream);
+
+/*
+ * The whole layer, fused: router/top-k, permutation, grouped gate/up with the
+ * clamped SwiGLU epilogue, grouped down whose epilogue multiplies by the
+ * routing weight and adds into out (fp32 [T][H], overwritten), with the
+ * shared expert run as one more group of weight 1.  The fp32 additions into
+ * out are atomic, so the last bits may differ run to run.
+ */
+moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_router,
+                           const float* b_router, const moe_weights* experts,
+                           const moe_weights* shared, float* out, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/*
+ * Stage boundaries of moe_ffn_forward_timed: ev[i] is recorded on `stream`
+ * before stage i, ev[MOE_STAGE_COUNT] after the last one.  Stages:
+ *   0 router logits + top-k      1 permutation (count, scan, scatter, gather)
+ *   2 grouped gate/up + SwiGLU   3 grouped down + weighted scatter-add
+ * Each ev[i] is a cudaEvent_t created by the caller (NULL entries are skipped).
+ */
+#define MOE_STAGE_COUNT 4
+typedef struct moe_stage_events {
+  void* ev[MOE_STAGE_COUNT + 1];
+} moe_stage_events;
+
+/*
+ * moe_ffn_forward with CUDA events recorded between its stages, so that a
+ * caller can time each kernel on the launching stream.  Same arguments and
+ * results as moe_ffn_forward; `events` may be NULL.
+ */
+moe_status moe_ffn_forward_timed(const moe_dims* d, const void* x, const void* w_router,
+                                 const float* b_router, const moe_weights* experts,
+                                 const moe_weights* shared, float* out, void* ws,
+                                 size_t ws_bytes, const moe_stage_events* events,
+                                 moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, returns the device status word that kernels using
+ * this workspace have set (MOE_OK, or MOE_ERR_TIMEOUT when a bounded
+ * device-side wait gave up), and clears it.
+ */
+moe_status moe_workspace_status(void* ws, moe_stream_t stream);
+
+/*
+ * Diagnostic: runs one device-side bounded wait on a barrier that nothing
+ * completes, with a budget of `budget_ns`, so that the timeout path can be
+ * exercised without a fault.  Sets the workspace status to MOE_ERR_TIMEOUT.
+ * ws must hold at least 256 bytes.
+ */
+moe_status moe_debug_wait_timeout(void* ws, uint64_t budget_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

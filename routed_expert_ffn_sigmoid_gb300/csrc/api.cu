@@ -1,0 +1,479 @@
+// C ABI of the MoE FFN layer: argument checks, workspace layout, TMA tensor
+// maps and the launch sequence of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/moe_ffn.h"
+#include "moe_kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;        // status word + reserved
+constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many tokens
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, total;
+};
+
+int rows_of(const moe_dims& d) { return (d.top_k + 1) * d.T; }
+
+int pick_bn(int T) {
+  if (T <= 16) return 16;
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  return 128;
+}
+
+size_t table_bytes(const moe_dims& d) {
+  // every group contributes at most ceil(cnt / 16) entries; the sum is
+  // bounded by (E + 1) + rows / 16
+  const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 15) / 16;
+  return kTableHeaderBytes + entries * sizeof(TileEntry);
+}
+
+Layout layout_of(const moe_dims& d) {
+  Layout L{};
+  const size_t T = d.T, E = d.E, k = d.top_k, H = d.H, I = d.I, rows = rows_of(d);
+  const size_t nblk = (T + kPermTokBlock - 1) / kPermTokBlock;
+  size_t o = kHeaderBytes;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.z = take(T * E * 4);
+  L.idx = take(T * k * 4);
+  L.w = take(T * k * 4);
+  L.blockcnt = take(nblk * E * 4);
+  L.offsets = take((E + 2) * 4);
+  L.table = take(table_bytes(d));
+  L.gather = take(rows * 4);
+  L.row_of = take(T * k * 4);
+  L.roww = take(rows * 4);
+  L.x_perm = take(rows * H * 2);
+  L.h0 = take(rows * I * 2);
+  L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
+  L.total = o;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->I <= 0 || d->I_shared <= 0 || d->top_k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->fmt != MOE_W_BF16 && d->fmt != MOE_W_INT4_G32) return MOE_ERR_UNSUPPORTED;
+  if (d->H % 128 != 0 || d->H > 12288) return MOE_ERR_UNSUPPORTED;
+  if (d->I % 64 != 0 || d->I_shared != d->I) return MOE_ERR_UNSUPPORTED;
+  if (d->E > kMaxE || d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->T) * (d->top_k + 1) > (1 << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// K-major operand of 16-bit elements [d2][d1][d0] (d0 = reduction, innermost),
+// box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+bool encode_kmajor(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_t d1,
+                   uint64_t d2, uint32_t box_rows) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t rank = d2 > 1 ? 3 : 2;
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weight stacks are always addressed as 3-D maps (a 2-D map ignores the third
+// coordinate, so the shared expert's leading dimension of 1 is fine).
+bool encode_weights(CUtensorMap* m, const void* base, bool bf16, uint64_t K, uint64_t N,
+                    uint64_t n_experts) {
+  const uint32_t box_rows = N < 128 ? static_cast<uint32_t>(N) : 128u;
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {K, N, n_experts};
+  const cuuint64_t strides[2] = {K * 2, K * N * 2};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool weights_ok(const moe_weights* w, int fmt) {
+  if (!w || !w->gate || !w->up || !w->down) return false;
+  if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return false;
+  if (fmt == MOE_W_INT4_G32) {
+    if (!w->gate_scale || !w->up_scale || !w->down_scale) return false;
+    if (!aligned16(w->gate_scale) || !aligned16(w->up_scale) || !aligned16(w->down_scale))
+      return false;
+  }
+  return true;
+}
+
+struct Ws {
+  char* base;
+  Layout L;
+  int* status() const { return reinterpret_cast<int*>(base); }
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(base + off);
+  }
+};
+
+moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes, Ws* out) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  out->L = layout_of(d);
+  if (ws_bytes < out->L.total) return MOE_ERR_WORKSPACE;
+  out->base = static_cast<char*>(ws);
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ stages
+
+moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
+                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
+  float* z = ws.at<float>(ws.L.z);
+  cudaError_t e;
+  if (d.T >= kRouterTcMinTokens) {
+    DownLaunch L{};
+    if (!encode_weights(&L.tm_a, w_router, true, d.H, d.E, 1) ||
+        !encode_kmajor(&L.tm_b0, x, true, d.H, d.T, 1, 16))
+      return MOE_ERR_CUDA;
+    L.tm_a_shared = L.tm_a;
+    L.tm_b1 = L.tm_b0;
+    L.table = nullptr;
+    L.dense_rows = d.T;
+    L.BN = 128;
+    L.nb = 1;
+    L.K = d.H;
+    L.N_out = d.E;
+    L.mblocks = (d.E + 127) / 128;
+    L.E = -1;
+    L.a_rows = d.E < 128 ? d.E : 128;
+    L.total_rows = d.T;
+    L.out_rows = d.T;
+    L.bf16 = true;
+    L.epilogue = kEpiRouter;
+    L.bias = b;
+    L.out = z;
+    L.status = ws.status();
+    L.budget_ns = kWaitBudgetNs;
+    const int tiles = ((d.T + 127) / 128) * L.mblocks;
+    L.grid = tiles < sm_count() ? tiles : sm_count();
+    e = launch_down(L, s);
+  } else {
+    e = launch_router_logits_simt(static_cast<const uint16_t*>(x),
+                                  static_cast<const uint16_t*>(w_router), b, z, d.T, d.H, d.E, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return from_cuda(launch_topk(z, d.T, d.E, d.top_k, idx, w, s));
+}
+
+moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, const void* x,
+                       int32_t* offsets, int32_t* gather, int32_t* row_of, float* roww,
+                       void* x_perm, int32_t* table, const Ws& ws, cudaStream_t s) {
+  int32_t* blockcnt = ws.at<int32_t>(ws.L.blockcnt);
+  cudaError_t e = launch_perm_count(idx, d.T, d.E, d.top_k, blockcnt, s);
+  if (e == cudaSuccess)
+    e = launch_perm_scan(blockcnt, d.T, d.E, d.top_k, offsets, table, pick_bn(d.T), s);
+  if (e == cudaSuccess)
+    e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(d), d.H, d.T,
+                           d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), s);
+  return from_cuda(e);
+}
+
+// Grouped gate/up + down over the permuted rows described by `table`.
+void record(const moe_stage_events* ev, int i, cudaStream_t s) {
+  if (ev && ev->ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev->ev[i]), s);
+}
+
+moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* table,
+                       const moe_weights* ex, const moe_weights* sh, int epilogue,
+                       const int32_t* gather, const float* roww, float* out, const Ws& ws,
+                       cudaStream_t s, const moe_stage_events* ev = nullptr) {
+  if (d.fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;  // Int4 grouped GEMM: see below
+  const int rows = rows_of(d);
+  const int BN = pick_bn(d.T);
+  const int nsm = sm_count();
+  const int max_entries = (d.E + 1) + (rows + BN - 1) / BN;
+
+  GateUpLaunch G{};
+  const bool bf16 = true;
+  if (!encode_weights(&G.tm_gate, ex->gate, bf16, d.H, d.I, d.E) ||
+      !encode_weights(&G.tm_up, ex->up, bf16, d.H, d.I, d.E) ||
+      !encode_weights(&G.tm_sgate, sh->gate, bf16, d.H, d.I, 1) ||
+      !encode_weights(&G.tm_sup, sh->up, bf16, d.H, d.I, 1) ||
+      !encode_kmajor(&G.tm_x, x_perm, bf16, d.H, rows, 1, 16))
+    return MOE_ERR_CUDA;
+  G.table = table;
+  G.BN = BN;
+  G.K = d.H;
+  G.I = d.I;
+  G.E = d.E;
+  G.a_rows = d.I < 128 ? d.I : 128;
+  G.total_rows = rows;
+  G.bf16 = bf16;
+  G.h0 = ws.at<void>(ws.L.h0);
+  G.h1 = ws.at<void>(ws.L.h1);
+  G.status = ws.status();
+  G.budget_ns = kWaitBudgetNs;
+  {
+    const int tiles = max_entries * ((d.I + 127) / 128);
+    G.grid = tiles < nsm ? tiles : nsm;
+  }
+  record(ev, 2, s);
+  cudaError_t e = launch_gateup(G, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(ev, 3, s);
+
+  DownLaunch D{};
+  if (!encode_weights(&D.tm_a, ex->down, bf16, d.I, d.H, d.E) ||
+      !encode_weights(&D.tm_a_shared, sh->down, bf16, d.I, d.H, 1) ||
+      !encode_kmajor(&D.tm_b0, G.h0, true, d.I, rows, 1, 16) ||
+      !encode_kmajor(&D.tm_b1, G.h1, true, d.I, rows, 1, 16))
+    return MOE_ERR_CUDA;
+  D.table = table;
+  D.dense_rows = 0;
+  D.BN = BN;
+  D.nb = 2;
+  D.K = d.I;
+  D.N_out = d.H;
+  D.mblocks = d.H / 128;
+  D.E = d.E;
+  D.a_rows = 128;
+  D.total_rows = rows;
+  D.out_rows = d.T;
+  D.bf16 = true;
+  D.epilogue = epilogue;
+  D.gather = gather;
+  D.roww = roww;
+  D.bias = nullptr;
+  D.out = out;
+  D.status = ws.status();
+  D.budget_ns = kWaitBudgetNs;
+  {
+    const int tiles = max_entries * D.mblocks;
+    D.grid = tiles < nsm ? tiles : nsm;
+  }
+  e = launch_down(D, s);
+  record(ev, 4, s);
+  return from_cuda(e);
+}
+
+moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
+                        const float* b_router, const moe_weights* experts,
+                        const moe_weights* shared, float* out, void* ws, size_t ws_bytes,
+                        const moe_stage_events* ev, moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // nothing is read or written
+  if (!x || !w_router || !b_router || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(experts, d->fmt) || !weights_ok(shared, d->fmt)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  if (d->fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Layout& L = w.L;
+  record(ev, 0, s);
+  if (cudaMemsetAsync(out, 0, static_cast<size_t>(d->T) * d->H * sizeof(float), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int32_t* idx = w.at<int32_t>(L.idx);
+  float* wts = w.at<float>(L.w);
+  if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
+  record(ev, 1, s);
+  int32_t* gather = w.at<int32_t>(L.gather);
+  float* roww = w.at<float>(L.roww);
+  int32_t* table = w.at<int32_t>(L.table);
+  void* x_perm = w.at<void>(L.x_perm);
+  if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of),
+                        roww, x_perm, table, w, s)) != MOE_OK)
+    return st;
+  return run_experts(*d, x_perm, table, experts, shared, kEpiScatterAdd, gather, roww, out, w, s,
+                     ev);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_FFN_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null, misaligned or negative argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape, format or GPU not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_size()";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device-side wait ran out of time";
+  }
+  return "unknown moe_status";
+}
+
+size_t moe_workspace_size(const moe_dims* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout_of(*d).total;
+}
+
+moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_router,
+                           const float* b_router, int32_t* topk_idx, float* topk_w, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // nothing is read or written
+  if (!x || !w_router || !b_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  return run_router(*d, x, w_router, b_router, topk_idx, topk_w, w,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, const void* x,
+                       int32_t* offsets, int32_t* gather, int32_t* row_of, void* x_perm, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // nothing is read or written
+  if (!topk_idx || !x || !offsets || !gather || !row_of || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  return run_permute(*d, topk_idx, nullptr, x, offsets, gather, row_of, nullptr, x_perm,
+                     w.at<int32_t>(w.L.table), w, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* offsets,
+                          const moe_weights* experts, const moe_weights* shared, float* y_perm,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // nothing is read or written
+  if (!x_perm || !offsets || !y_perm || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(experts, d->fmt) || !weights_ok(shared, d->fmt)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  if (d->fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* table = w.at<int32_t>(w.L.table);
+  const int capacity =
+      static_cast<int>((table_bytes(*d) - kTableHeaderBytes) / sizeof(TileEntry));
+  if (launch_table_from_offsets(offsets, d->E, rows_of(*d), capacity, table, pick_bn(d->T), s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return run_experts(*d, x_perm, table, experts, shared, kEpiStoreRows, nullptr, nullptr, y_perm,
+                     w, s);
+}
+
+moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* row_of,
+                       const float* topk_w, float* out, moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // nothing is read or written
+  if (!y_perm || !row_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_combine(y_perm, row_of, topk_w, d->T, d->H, d->top_k, out,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_router,
+                           const float* b_router, const moe_weights* experts,
+                           const moe_weights* shared, float* out, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+  return forward_impl(d, x, w_router, b_router, experts, shared, out, ws, ws_bytes, nullptr,
+                      stream);
+}
+
+moe_status moe_ffn_forward_timed(const moe_dims* d, const void* x, const void* w_router,
+                                 const float* b_router, const moe_weights* experts,
+                                 const moe_weights* shared, float* out, void* ws,
+                                 size_t ws_bytes, const moe_stage_events* events,
+                                 moe_stream_t stream) {
+  return forward_impl(d, x, w_router, b_router, experts, shared, out, ws, ws_bytes, events,
+                      stream);
+}
+
+moe_status moe_workspace_status(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int code = 0;
+  if (cudaMemcpyAsync(&code, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (code != 0 && cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return code == 0 ? MOE_OK : (code == kStatusTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA);
+}
+
+moe_status moe_debug_wait_timeout(void* ws, uint64_t budget_ns, moe_stream_t stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return from_cuda(launch_wait_selftest(static_cast<int*>(ws), budget_ns,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,624 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands streamed by TMA through an mbarrier ring.
+//
+// Per-expert gate / up / down matmuls ("ggml_mul_mat_id" for gate, up and
+// down; clamped SwiGLU between gate/up and down; shared expert combined with
+// the routed output -- "Add GLM-5.3-Flash (glm5next) support with ROCmFP mix
+// qtypes (105/106)", section "MoE FFN (REAL routed expert execution)").
+//
+// Orientation ("swap AB"): the weight rows are the M = 128 operand and the
+// tokens of one expert group are the N operand (16..256, chosen per tile), so
+// a group of a few decode tokens still issues full-height MMAs and each
+// weight byte crosses HBM once.  D[feature][token] accumulates in TMEM.
+//
+// CTA = 6 warps, persistent over a flat tile list:
+//   warp 0, lane 0  TMA producer (weights evict-first, activations evict-last)
+//   warp 1          TMEM allocation; lane 0 issues tcgen05.mma, commits
+//   warps 2..5      epilogue: tcgen05.ld of their 32-lane TMEM quadrant
+// Accumulators are double-buffered in TMEM where they fit, so the epilogue of
+// one tile overlaps the main loop of the next.
+//
+// Every wait is bounded (AbortState): on a timeout the CTA records
+// MOE_ERR_TIMEOUT in the workspace status word, drains the copies and MMAs it
+// issued, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "moe_kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;                      // MMA M: weight rows per tile
+constexpr int kBK = 64;                       // K per stage: one 128-byte swizzle row
+constexpr int kRowBytes = kBK * 2;            // 128
+constexpr int kChunkRows = 16;                // token rows per activation TMA box
+constexpr int kChunkBytes = kChunkRows * kRowBytes;
+constexpr int kATileBytes = kBM * kRowBytes;  // 16 KB
+constexpr int kStageBudget = 224 * 1024;
+constexpr int kThreads = 192;
+
+constexpr int ceil_pow2_32(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+template <int BN>
+struct GateUpCfg {
+  static constexpr int kBTileBytes = BN * kRowBytes;
+  static constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes;
+  static constexpr int kStages = cmin(8, kStageBudget / kStageBytes);
+  static constexpr int kAccStages = (4 * BN <= 512) ? 2 : 1;
+  static constexpr int kAccCols = 2 * BN;  // gate accumulator, then up accumulator
+  static constexpr int kTmemCols = ceil_pow2_32(kAccStages * kAccCols);
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+};
+
+template <int BN, int NB>
+struct DownCfg {
+  static constexpr int kBTileBytes = BN * kRowBytes;
+  static constexpr int kStageBytes = kATileBytes + NB * kBTileBytes;
+  static constexpr int kStages = cmin(8, kStageBudget / kStageBytes);
+  static constexpr int kAccStages = (2 * BN <= 512) ? 2 : 1;
+  static constexpr int kTmemCols = ceil_pow2_32(kAccStages * BN);
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+};
+
+struct GateUpArgs {
+  const int32_t* table;
+  int K, I, E, a_rows, total_rows;
+  void* h0;
+  void* h1;
+  int* status;
+  uint64_t budget_ns;
+};
+
+struct DownArgs {
+  const int32_t* table;
+  int dense_rows;
+  int K, N_out, mblocks, E, a_rows, total_rows, out_rows;
+  const int32_t* gather;
+  const float* roww;
+  const float* bias;
+  float* out;
+  int* status;
+  uint64_t budget_ns;
+};
+
+__device__ __forceinline__ int n_entries_of(const int32_t* table, int dense_rows, int BN) {
+  return table ? table[0] : (dense_rows + BN - 1) / BN;
+}
+
+__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int dense_rows, int BN, int i) {
+  if (table) {
+    const int4 v = reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) +
+                                                 kTableHeaderBytes)[i];
+    return TileEntry{v.x, v.y, v.z, v.w};
+  }
+  return TileEntry{0, i * BN, min(BN, dense_rows - i * BN), 0};
+}
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// silu(min(g, 10)) * clamp(u, -10, 10)
+__device__ __forceinline__ float clamped_swiglu(float g, float u) {
+  const float gc = fminf(g, 10.0f);
+  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
+  return gc / (1.0f + expf(-gc)) * uc;
+}
+
+struct SmemCarve {
+  uint8_t* tiles;
+  uint64_t *full, *empty, *tfull, *tempty, *drain;
+  uint32_t* tmem_holder;
+  int* abort_flag;
+};
+
+__device__ __forceinline__ SmemCarve carve(uint8_t* raw, int stages, int stage_bytes) {
+  SmemCarve c;
+  c.tiles = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  c.full = reinterpret_cast<uint64_t*>(c.tiles + stages * stage_bytes);
+  c.empty = c.full + stages;
+  c.tfull = c.empty + stages;
+  c.tempty = c.tfull + 2;
+  c.drain = c.tempty + 2;
+  c.tmem_holder = reinterpret_cast<uint32_t*>(c.drain + 1);
+  c.abort_flag = reinterpret_cast<int*>(c.tmem_holder + 1);
+  return c;
+}
+
+__device__ __forceinline__ void init_barriers(const SmemCarve& c, int stages) {
+  for (int s = 0; s < stages; ++s) {
+    mbar_init(&c.full[s], 1);
+    mbar_init(&c.empty[s], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&c.tfull[i], 1);
+    mbar_init(&c.tempty[i], 128);
+  }
+  mbar_init(c.drain, 1);
+  *c.abort_flag = 0;
+  fence_barrier_init();
+}
+
+// ======================================================================
+// gate/up: D_g = W_gate[e] x X^T, D_u = W_up[e] x X^T, then the clamped
+// SwiGLU.  bf16 path: h is stored as a hi/lo pair of bf16 planes (h = hi +
+// lo to ~16 bits), which keeps the down projection's input error far below
+// a bf16 rounding while the down MMA still takes bf16 operands.  fp16 path
+// (Int4 weights): h is stored as one fp16 plane.
+// ======================================================================
+template <int BN, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gateup_kernel(const __grid_constant__ CUtensorMap tm_gate,
+                  const __grid_constant__ CUtensorMap tm_up,
+                  const __grid_constant__ CUtensorMap tm_sgate,
+                  const __grid_constant__ CUtensorMap tm_sup,
+                  const __grid_constant__ CUtensorMap tm_x, const GateUpArgs a) {
+  using Cfg = GateUpCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const SmemCarve sm = carve(smem_raw, Cfg::kStages, Cfg::kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    init_barriers(sm, Cfg::kStages);
+    tma_prefetch_desc(&tm_gate);
+    tma_prefetch_desc(&tm_up);
+    tma_prefetch_desc(&tm_sgate);
+    tma_prefetch_desc(&tm_sup);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *sm.tmem_holder;
+  const AbortState ab{sm.abort_flag, a.status, a.budget_ns};
+
+  pdl_wait();
+  pdl_launch_dependents();
+  const int mblocks = (a.I + kBM - 1) / kBM;
+  const int total = n_entries_of(a.table, 0, BN) * mblocks;
+  const int KB = a.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+        const int mb = tile % mblocks;
+        const bool sh = te.group == a.E;
+        const CUtensorMap* mg = sh ? &tm_sgate : &tm_gate;
+        const CUtensorMap* mu = sh ? &tm_sup : &tm_up;
+        const int ge = sh ? 0 : te.group;
+        const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
+        const uint32_t bytes = 2u * a.a_rows * kRowBytes + nchunks * kChunkBytes;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = sm.tiles + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&sm.full[stage], bytes);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_3d(st, mg, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
+          tma_load_3d(st + kATileBytes, mu, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
+          for (int c = 0; c < nchunks; ++c)
+            tma_load_2d(st + 2 * kATileBytes + c * kChunkBytes, &tm_x, &sm.full[stage], kb * kBK,
+                        te.row0 + c * kChunkRows, pol_x);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int s = 0; s < Cfg::kStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&sm.full[s], (armed_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_f16(kBM, 16, kBf16) & ~(0x3Fu << 17);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+        const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
+        if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, ab)) break;
+        tc_fence_after_sync();
+        const uint32_t d_g = tmem_base + acc * Cfg::kAccCols;
+        const uint32_t d_u = d_g + BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = smem_u32(sm.tiles + stage * Cfg::kStageBytes);
+          const uint64_t dg = sw128_kmajor_desc(st);
+          const uint64_t du = sw128_kmajor_desc(st + kATileBytes);
+          const uint64_t db = sw128_kmajor_desc(st + 2 * kATileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t accum = (kb | k) != 0;
+            umma_f16(d_g, dg + 2 * k, db + 2 * k, idesc, accum);
+            umma_f16(d_u, du + 2 * k, db + 2 * k, idesc, accum);
+          }
+          umma_commit(&sm.empty[stage]);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sm.tfull[acc]);
+        if (Cfg::kAccStages == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued has completed before TMEM is freed
+      umma_commit(sm.drain);
+      mbar_wait_drain(sm.drain, 0);
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+      const int mb = tile % mblocks;
+      // warp-uniform outcome: tcgen05.ld below is .sync.aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.tfull[acc], acc_phase, ab))) break;
+      tc_fence_after_sync();
+      const int f = mb * kBM + q * 32 + lane;
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
+      const int n = round16(te.nrows);
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        uint32_t g[16], u[16];
+        tmem_ld_32x32b_x16(tq + c0, g);
+        tmem_ld_32x32b_x16(tq + BN + c0, u);
+        tmem_ld_wait();
+        if (f < a.I) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            if (c < te.nrows && te.row0 + c < a.total_rows) {
+              const float hv = clamped_swiglu(__uint_as_float(g[i]), __uint_as_float(u[i]));
+              const size_t o = static_cast<size_t>(te.row0 + c) * a.I + f;
+              if (kBf16) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                static_cast<__nv_bfloat16*>(a.h0)[o] = hi;
+                static_cast<__nv_bfloat16*>(a.h1)[o] = lo;
+              } else {
+                static_cast<__half*>(a.h0)[o] = __float2half_rn(hv);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&sm.tempty[acc]);
+      if (Cfg::kAccStages == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ======================================================================
+// Single-A GEMM: D = W[e] x B^T with one or two B operands per k-step
+// (two = the hi/lo planes of h, summed into one accumulator).  Epilogues:
+//   scatter-add  out[gather[r]][f] += roww[r] * D     (down, fused layer)
+//   store rows   out[r][f] = D                         (down, y_perm)
+//   router       out[r][f] = D + bias[f]               (router logits)
+// ======================================================================
+template <int BN, int NB, bool kBf16, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    down_kernel(const __grid_constant__ CUtensorMap tm_a,
+                const __grid_constant__ CUtensorMap tm_a_shared,
+                const __grid_constant__ CUtensorMap tm_b0,
+                const __grid_constant__ CUtensorMap tm_b1, const DownArgs a) {
+  using Cfg = DownCfg<BN, NB>;
+  extern __shared__ uint8_t smem_raw[];
+  const SmemCarve sm = carve(smem_raw, Cfg::kStages, Cfg::kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    init_barriers(sm, Cfg::kStages);
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a_shared);
+    tma_prefetch_desc(&tm_b0);
+    if (NB == 2) tma_prefetch_desc(&tm_b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *sm.tmem_holder;
+  const AbortState ab{sm.abort_flag, a.status, a.budget_ns};
+
+  pdl_wait();
+  pdl_launch_dependents();
+  const int total = n_entries_of(a.table, a.dense_rows, BN) * a.mblocks;
+  const int KB = a.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
+        const int mb = tile % a.mblocks;
+        const bool sh = te.group == a.E;
+        const CUtensorMap* ma = sh ? &tm_a_shared : &tm_a;
+        const int ge = sh ? 0 : te.group;
+        const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
+        const uint32_t bytes = a.a_rows * kRowBytes + NB * nchunks * kChunkBytes;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = sm.tiles + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&sm.full[stage], bytes);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_3d(st, ma, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
+          for (int c = 0; c < nchunks; ++c) {
+            tma_load_2d(st + kATileBytes + c * kChunkBytes, &tm_b0, &sm.full[stage], kb * kBK,
+                        te.row0 + c * kChunkRows, pol_x);
+            if (NB == 2)
+              tma_load_2d(st + kATileBytes + Cfg::kBTileBytes + c * kChunkBytes, &tm_b1,
+                          &sm.full[stage], kb * kBK, te.row0 + c * kChunkRows, pol_x);
+          }
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < Cfg::kStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&sm.full[s], (armed_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_f16(kBM, 16, kBf16) & ~(0x3Fu << 17);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
+        const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
+        if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, ab)) break;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = smem_u32(sm.tiles + stage * Cfg::kStageBytes);
+          const uint64_t da = sw128_kmajor_desc(st);
+          const uint64_t db0 = sw128_kmajor_desc(st + kATileBytes);
+          const uint64_t db1 = sw128_kmajor_desc(st + kATileBytes + Cfg::kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            umma_f16(d, da + 2 * k, db0 + 2 * k, idesc, (kb | k) != 0);
+            if (NB == 2) umma_f16(d, da + 2 * k, db1 + 2 * k, idesc, 1u);
+          }
+          umma_commit(&sm.empty[stage]);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sm.tfull[acc]);
+        if (Cfg::kAccStages == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit(sm.drain);
+      mbar_wait_drain(sm.drain, 0);
+    }
+  } else {
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
+      const int mb = tile % a.mblocks;
+      // warp-uniform outcome: tcgen05.ld below is .sync.aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.tfull[acc], acc_phase, ab))) break;
+      tc_fence_after_sync();
+      const int f = mb * kBM + q * 32 + lane;
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int n = round16(te.nrows);
+      const float fbias = (EPI == kEpiRouter && f < a.N_out) ? a.bias[f] : 0.f;
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tq + c0, v);
+        tmem_ld_wait();
+        if (f < a.N_out) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            const int r = te.row0 + c;
+            if (c < te.nrows && r < a.total_rows) {
+              const float d = __uint_as_float(v[i]);
+              if (EPI == kEpiScatterAdd) {
+                const int t = a.gather[r];
+                if (t >= 0 && t < a.out_rows)
+                  atomicAdd(a.out + static_cast<size_t>(t) * a.N_out + f, a.roww[r] * d);
+              } else if (EPI == kEpiStoreRows) {
+                a.out[static_cast<size_t>(r) * a.N_out + f] = d;
+              } else {
+                a.out[static_cast<size_t>(r) * a.N_out + f] = d + fbias;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&sm.tempty[acc]);
+      if (Cfg::kAccStages == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+__global__ void wait_selftest_kernel(int* status, uint64_t budget_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const AbortState ab{&flag, status, budget_ns};
+    mbar_wait(&bar, 0, ab);  // nothing arrives: runs out of budget
+  }
+}
+
+template <int BN, bool kBf16>
+cudaError_t gateup_dispatch(const GateUpLaunch& L, cudaStream_t s) {
+  using Cfg = GateUpCfg<BN>;
+  auto kern = gateup_kernel<BN, kBf16>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  GateUpArgs a{L.table, L.K, L.I, L.E, L.a_rows, L.total_rows, L.h0, L.h1, L.status,
+               L.budget_ns};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_gate, L.tm_up, L.tm_sgate, L.tm_sup, L.tm_x, a);
+}
+
+template <int BN, int NB, bool kBf16, int EPI>
+cudaError_t down_dispatch(const DownLaunch& L, cudaStream_t s) {
+  using Cfg = DownCfg<BN, NB>;
+  auto kern = down_kernel<BN, NB, kBf16, EPI>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  DownArgs a{L.table, L.dense_rows, L.K, L.N_out, L.mblocks, L.E, L.a_rows, L.total_rows,
+             L.out_rows, L.gather, L.roww, L.bias, L.out, L.status, L.budget_ns};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_a, L.tm_a_shared, L.tm_b0, L.tm_b1, a);
+}
+
+template <int NB, bool kBf16, int EPI>
+cudaError_t down_by_bn(const DownLaunch& L, cudaStream_t s) {
+  switch (L.BN) {
+    case 16: return down_dispatch<16, NB, kBf16, EPI>(L, s);
+    case 32: return down_dispatch<32, NB, kBf16, EPI>(L, s);
+    case 64: return down_dispatch<64, NB, kBf16, EPI>(L, s);
+    case 128: return down_dispatch<128, NB, kBf16, EPI>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const GateUpLaunch& L, cudaStream_t s) {
+  if (L.bf16) {
+    switch (L.BN) {
+      case 16: return gateup_dispatch<16, true>(L, s);
+      case 32: return gateup_dispatch<32, true>(L, s);
+      case 64: return gateup_dispatch<64, true>(L, s);
+      case 128: return gateup_dispatch<128, true>(L, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (L.BN) {
+    case 16: return gateup_dispatch<16, false>(L, s);
+    case 32: return gateup_dispatch<32, false>(L, s);
+    case 64: return gateup_dispatch<64, false>(L, s);
+    case 128: return gateup_dispatch<128, false>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_down(const DownLaunch& L, cudaStream_t s) {
+  if (L.epilogue == kEpiRouter) {
+    if (!L.bf16 || L.nb != 1) return cudaErrorInvalidValue;
+    return down_by_bn<1, true, kEpiRouter>(L, s);
+  }
+  if (L.bf16) {
+    if (L.nb != 2) return cudaErrorInvalidValue;
+    return L.epilogue == kEpiScatterAdd ? down_by_bn<2, true, kEpiScatterAdd>(L, s)
+                                        : down_by_bn<2, true, kEpiStoreRows>(L, s);
+  }
+  if (L.nb != 1) return cudaErrorInvalidValue;
+  return L.epilogue == kEpiScatterAdd ? down_by_bn<1, false, kEpiScatterAdd>(L, s)
+                                      : down_by_bn<1, false, kEpiStoreRows>(L, s);
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t budget_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,108 @@
+// Internal launch interface between the C-ABI translation unit and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxE = 512;        // routed experts supported by router / permute
+constexpr int kMaxTopK = 16;
+constexpr int kPermTokBlock = 128; // tokens per counting-sort block
+constexpr int kTableHeaderBytes = 16;
+
+// One grouped-GEMM work entry: rows [row0, row0 + nrows) of group `group`
+// (group == E is the shared expert).  nrows <= the launch's token tile BN.
+struct TileEntry {
+  int32_t group, row0, nrows, pad;
+};
+
+// ---------------------------------------------------------------- router
+
+// z[t][e] = sum_h x[t][h] w_router[e][h] + b[e] on CUDA cores (fp32 FMA).
+cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_router, const float* b,
+                                      float* z, int T, int H, int E, cudaStream_t s);
+
+// Per token: top_k of z (ties to the lower index), sigmoid, renormalise.
+cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------- permute
+
+cudaError_t launch_perm_count(const int32_t* idx, int T, int E, int k, int32_t* blockcnt,
+                              cudaStream_t s);
+// Turns block counts into per-block row bases, writes offsets[E+2] and the
+// tile table (entries of at most BN rows).  One CTA.
+cudaError_t launch_perm_scan(int32_t* blockcnt, int T, int E, int k, int32_t* offsets,
+                             int32_t* table, int BN, cudaStream_t s);
+// Stable ranks inside each block; gather / row_of / row weights.
+cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_t* blockbase,
+                                int T, int E, int k, int32_t* gather, int32_t* row_of,
+                                float* roww, cudaStream_t s);
+// x_perm[r] = x[gather[r]]; to_fp16 converts bf16 -> fp16 on the way.
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
+                               bool to_fp16, uint16_t* x_perm, cudaStream_t s);
+// Tile table from existing offsets (for the unfused expert entry point);
+// at most `capacity` entries.
+cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,
+                                      int32_t* table, int BN, cudaStream_t s);
+
+// ---------------------------------------------------------------- combine
+
+cudaError_t launch_combine(const float* y_perm, const int32_t* row_of, const float* w, int T,
+                           int H, int k, float* out, cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped GEMMs
+
+struct GateUpLaunch {
+  CUtensorMap tm_gate, tm_up, tm_sgate, tm_sup, tm_x;
+  const int32_t* table;
+  int BN;            // token tile (16, 32, 64, 128, 256)
+  int K;             // H
+  int I;             // intermediate size (features)
+  int E;             // group id of the shared expert
+  int a_rows;        // rows of one weight box (min(128, I))
+  int total_rows;    // rows of x_perm / h (stores beyond are dropped)
+  bool bf16;         // bf16 operands (else fp16)
+  void* h0;          // bf16 path: hi plane; fp16 path: h
+  void* h1;          // bf16 path: lo plane; fp16 path: null
+  int* status;
+  uint64_t budget_ns;
+  int grid;
+};
+cudaError_t launch_gateup(const GateUpLaunch& L, cudaStream_t s);
+
+enum DownEpilogue : int { kEpiScatterAdd = 0, kEpiStoreRows = 1, kEpiRouter = 2 };
+
+struct DownLaunch {
+  CUtensorMap tm_a, tm_a_shared, tm_b0, tm_b1;
+  const int32_t* table;  // null: dense tiles over `dense_rows` rows, group 0
+  int dense_rows;
+  int BN;
+  int nb;            // B operands per k-step: 2 = split (hi + lo), 1 = single
+  int K;             // reduction length
+  int N_out;         // output features (H for down, E for the router)
+  int mblocks;       // ceil(N_out / 128)
+  int E;             // shared group id (-1 when there is none)
+  int a_rows;        // rows of one weight box
+  int total_rows;    // rows of the B operand (stores beyond are dropped)
+  int out_rows;      // scatter-add: tokens in out (gather ids beyond are dropped)
+  bool bf16;
+  int epilogue;      // DownEpilogue
+  const int32_t* gather;
+  const float* roww;
+  const float* bias;
+  float* out;        // scatter-add: [T][N_out]; store rows: [rows][N_out]
+  int* status;
+  uint64_t budget_ns;
+  int grid;
+};
+cudaError_t launch_down(const DownLaunch& L, cudaStream_t s);
+
+// Diagnostic bounded wait on a barrier nothing completes.
+cudaError_t launch_wait_selftest(int* status, uint64_t budget_ns, cudaStream_t s);
+
+}  // namespace moe

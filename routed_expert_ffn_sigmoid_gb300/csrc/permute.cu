@@ -1,0 +1,267 @@
+// Counting-sort permutation of (token, slot) pairs by expert.
+//
+// The grouping the per-expert matmuls run on ("ggml_mul_mat_id" for gate, up
+// and down in "Add GLM-5.3-Flash (glm5next) support with ROCmFP mix qtypes
+// (105/106)", section "MoE FFN (REAL routed expert execution)"), built as a
+// stable counting sort so that rows of one expert are ordered by token:
+//   1. per 128-token block, a shared-memory histogram of expert ids;
+//   2. one CTA turns the block histograms into per-block row bases and the
+//      exclusive offsets (the shared expert appended as group E with all T
+//      tokens), and cuts every group into tiles of at most BN rows;
+//   3. per block, a token bitmap per expert gives each pair its rank among
+//      the block's earlier tokens -> row = base + rank;
+//   4. x rows are gathered into permuted order with 16-byte loads.
+#include <cuda_fp16.h>
+
+#include "moe_kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWordsPerBlock = kPermTokBlock / 32;
+
+__global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restrict__ idx, int T,
+                                                         int E, int k,
+                                                         int32_t* __restrict__ blockcnt) {
+  __shared__ int cnt[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kPermTokBlock;
+  const int nt = min(kPermTokBlock, T - t0);
+  const int32_t* ib = idx + static_cast<size_t>(t0) * k;
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int e = ib[i];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);  // out-of-range ids are ignored
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// Exclusive scan of n values in shared memory by warp 0 (n <= a few hundred).
+__device__ void warp0_exclusive_scan(int* v, int n, int* total) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const int x = i < n ? v[i] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (i < n) v[i] = carry + incl - x;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) *total = carry;
+}
+
+// One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ blockcnt, int T,
+                                                         int E, int k,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ table, int BN) {
+  __shared__ int tot[kMaxE + 1];
+  __shared__ int off[kMaxE + 2];
+  __shared__ int ntile[kMaxE + 1];
+  __shared__ int n_entries;
+  __shared__ int total_rows;
+  const int nblk = (T + kPermTokBlock - 1) / kPermTokBlock;
+  // per expert: running sum over blocks (becomes the block-relative base)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const size_t p = static_cast<size_t>(b) * E + e;
+      const int c = blockcnt[p];
+      blockcnt[p] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  if (threadIdx.x == 0) tot[E] = T;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) off[g] = tot[g];
+  __syncthreads();
+  warp0_exclusive_scan(off, E + 1, &total_rows);
+  __syncthreads();
+  if (threadIdx.x == 0) off[E + 1] = total_rows;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E + 1; g += blockDim.x) offsets[g] = off[g];
+  // block bases become absolute rows
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int b = 0; b < nblk; ++b) blockcnt[static_cast<size_t>(b) * E + e] += off[e];
+  // tile table: group g is cut into ceil(cnt / BN) entries
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (tot[g] + BN - 1) / BN;
+  __syncthreads();
+  warp0_exclusive_scan(ntile, E + 1, &n_entries);
+  __syncthreads();
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int c = tot[g];
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      TileEntry te;
+      te.group = g;
+      te.row0 = off[g] + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = n_entries;
+}
+
+__global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __restrict__ idx,
+                                                           const float* __restrict__ w,
+                                                           const int32_t* __restrict__ blockbase,
+                                                           int T, int E, int k,
+                                                           int32_t* __restrict__ gather,
+                                                           int32_t* __restrict__ row_of,
+                                                           float* __restrict__ roww) {
+  __shared__ uint32_t bits[kMaxE][kWordsPerBlock];
+  for (int i = threadIdx.x; i < E * kWordsPerBlock; i += blockDim.x) (&bits[0][0])[i] = 0u;
+  __syncthreads();
+  const int t0 = blockIdx.x * kPermTokBlock;
+  const int nt = min(kPermTokBlock, T - t0);
+  const int32_t* ib = idx + static_cast<size_t>(t0) * k;
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int e = ib[i];
+    if (e >= 0 && e < E) atomicOr(&bits[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  const int32_t* base = blockbase + static_cast<size_t>(blockIdx.x) * E;
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int e = ib[i];
+    if (e < 0 || e >= E) continue;
+    int rank = __popc(bits[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+    for (int wd = 0; wd < (tl >> 5); ++wd) rank += __popc(bits[e][wd]);
+    const int r = base[e] + rank;
+    const int t = t0 + tl;
+    gather[r] = t;
+    row_of[static_cast<size_t>(t0) * k + i] = r;
+    if (roww) roww[r] = w[static_cast<size_t>(t0) * k + i];
+  }
+  // the shared expert's rows: every token, in order, after the routed rows
+  for (int tl = threadIdx.x; tl < nt; tl += blockDim.x) {
+    const int r = k * T + t0 + tl;
+    gather[r] = t0 + tl;
+    if (roww) roww[r] = 1.0f;
+  }
+}
+
+// One warp per row, grid-stride.  H is a multiple of 128, so a row is a whole
+// number of 16-byte chunks.
+template <bool kToFp16>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ gather,
+                                                          int rows, int H, int T,
+                                                          uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int chunks = H / 8;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const int t = gather[r];
+    const bool valid = t >= 0 && t < T;  // rows no pair claimed stay zero
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(valid ? t : 0) * H);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
+    for (int c = lane; c < chunks; c += 32) {
+      uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      if (kToFp16) {
+        uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __uint_as_float(wv[i] << 16);
+          const float hi = __uint_as_float(wv[i] & 0xFFFF0000u);
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          wv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      dst[c] = v;
+    }
+  }
+}
+
+// Tile table from an offsets array (E+2 entries), one CTA.  Offsets are
+// clamped into [0, rows] and made non-decreasing, and no more than
+// `capacity` entries are written, so inconsistent offsets cannot send a tile
+// outside the row range or the table outside its buffer.
+__global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t* __restrict__ offsets,
+                                                                  int E, int rows, int capacity,
+                                                                  int32_t* __restrict__ table,
+                                                                  int BN) {
+  __shared__ int lo[kMaxE + 1];
+  __shared__ int ntile[kMaxE + 1];
+  __shared__ int n_entries;
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int a = min(max(offsets[g], 0), rows);
+    const int b = min(max(offsets[g + 1], a), rows);
+    lo[g] = a;
+    ntile[g] = (b - a + BN - 1) / BN;
+  }
+  __syncthreads();
+  warp0_exclusive_scan(ntile, E + 1, &n_entries);
+  __syncthreads();
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int o = lo[g];
+    const int c = min(max(offsets[g + 1], o), rows) - o;
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      if (ntile[g] + i >= capacity) break;
+      TileEntry te;
+      te.group = g;
+      te.row0 = o + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = min(n_entries, capacity);
+}
+
+}  // namespace
+
+cudaError_t launch_perm_count(const int32_t* idx, int T, int E, int k, int32_t* blockcnt,
+                              cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  perm_count_kernel<<<(T + kPermTokBlock - 1) / kPermTokBlock, 256, 0, s>>>(idx, T, E, k,
+                                                                            blockcnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_scan(int32_t* blockcnt, int T, int E, int k, int32_t* offsets,
+                             int32_t* table, int BN, cudaStream_t s) {
+  perm_scan_kernel<<<1, 1024, 0, s>>>(blockcnt, T, E, k, offsets, table, BN);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_t* blockbase,
+                                int T, int E, int k, int32_t* gather, int32_t* row_of,
+                                float* roww, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  perm_scatter_kernel<<<(T + kPermTokBlock - 1) / kPermTokBlock, 256, 0, s>>>(
+      idx, w, blockbase, T, E, k, gather, row_of, roww);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
+                               bool to_fp16, uint16_t* x_perm, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int blocks = min((rows + 7) / 8, 152 * 8);
+  if (to_fp16)
+    gather_rows_kernel<true><<<blocks, 256, 0, s>>>(x, gather, rows, H, T, x_perm);
+  else
+    gather_rows_kernel<false><<<blocks, 256, 0, s>>>(x, gather, rows, H, T, x_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,
+                                      int32_t* table, int BN, cudaStream_t s) {
+  table_from_offsets_kernel<<<1, 1024, 0, s>>>(offsets, E, rows, capacity, table, BN);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,102 @@
+"""Device-side helpers for the GPU tests: upload seeded inputs, run the
+library's entry points, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import routed_expert_ffn_sigmoid_gb300 as moe
+
+TOL = {"bf16": 2e-3, "int4": 5e-3}
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def dev_u16(a: np.ndarray):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def dev_u8(a: np.ndarray):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def upload_matrices(d: dict):
+    out = {}
+    for k, v in d.items():
+        out[k] = dev_u8(v) if v.dtype == np.uint8 else dev_u16(v)
+    return out
+
+
+def weights_struct(dev: dict):
+    return moe.make_weights(dev["gate"], dev["up"], dev["down"], dev.get("gate_scale"),
+                            dev.get("up_scale"), dev.get("down_scale"))
+
+
+class DeviceLayer:
+    """A layer's inputs resident on the GPU plus a workspace for dims(T)."""
+
+    def __init__(self, inp):
+        torch = torch_mod()
+        wl = inp.wl
+        self.inp = inp
+        self.wl = wl
+        self.wr = dev_u16(inp.w_router)
+        self.b = torch.from_numpy(inp.b_router).cuda()
+        self.ex = upload_matrices(inp.experts)
+        self.sh = upload_matrices(inp.shared)
+        self.exw = weights_struct(self.ex)
+        self.shw = weights_struct(self.sh)
+
+    def dims(self, T):
+        wl = self.wl
+        return moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
+
+    def workspace(self, T):
+        torch = torch_mod()
+        return torch.zeros(moe.moe_workspace_size(self.dims(T)), dtype=torch.uint8,
+                           device="cuda")
+
+    def forward(self, x_np: np.ndarray):
+        torch = torch_mod()
+        T = x_np.shape[0]
+        dims = self.dims(T)
+        ws = self.workspace(T)
+        x = dev_u16(x_np)
+        out = torch.empty((T, self.wl.H), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(dims, x, self.wr, self.b, self.exw, self.shw, out, ws)
+        st = moe.moe_workspace_status(ws)
+        assert st == moe.MOE_OK, moe.moe_status_string(st)
+        return out.cpu().numpy()
+
+    def router(self, x_np: np.ndarray):
+        torch = torch_mod()
+        T = x_np.shape[0]
+        dims = self.dims(T)
+        ws = self.workspace(T)
+        idx = torch.empty((T, self.wl.top_k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, self.wl.top_k), dtype=torch.float32, device="cuda")
+        moe.moe_router_topk(dims, dev_u16(x_np), self.wr, self.b, idx, w, ws)
+        torch.cuda.synchronize()
+        return idx.cpu().numpy(), w.cpu().numpy()
+
+
+def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, z_ref):
+    """Expert sets bit-exact; slot order where the oracle's adjacent logits
+    differ by more than 1e-4; weights per expert id within 1e-5 relative."""
+    T, k = idx_ref.shape
+    for t in range(T):
+        assert sorted(idx_gpu[t].tolist()) == sorted(idx_ref[t].tolist()), f"token {t}"
+        zs = z_ref[t, idx_ref[t]]
+        for j in range(k):
+            clear_before = j == 0 or zs[j - 1] - zs[j] > 1e-4
+            clear_after = j == k - 1 or zs[j] - zs[j + 1] > 1e-4
+            if clear_before and clear_after:
+                assert idx_gpu[t, j] == idx_ref[t, j], f"token {t} slot {j}"
+        ref_by_e = dict(zip(idx_ref[t].tolist(), w_ref[t].tolist()))
+        for j in range(k):
+            e = int(idx_gpu[t, j])
+            assert abs(w_gpu[t, j] - ref_by_e[e]) <= 1e-5 * ref_by_e[e] + 1e-7, f"token {t} e {e}"

@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI library (no GPU needed): it loads, exports
+every symbol the header declares, sizes workspaces, and rejects bad
+arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import routed_expert_ffn_sigmoid_gb300 as moe
+from routed_expert_ffn_sigmoid_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_ffn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    cuda_build.build()
+    return moe.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert set(names) == set(moe.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.moe_abi_version() == 1
+    for code in range(6):
+        assert moe.moe_status_string(code).startswith("MOE_")
+    assert "unknown" in moe.moe_status_string(42)
+
+
+def test_workspace_size(L):
+    d = moe.make_dims(64, 4096, 288, 1536)
+    small = moe.moe_workspace_size(moe.make_dims(1, 4096, 288, 1536))
+    big = moe.moe_workspace_size(d)
+    assert 0 < small < big
+    rows = 9 * 64
+    # at least x_perm + the two bf16 planes of h
+    assert big >= rows * 4096 * 2 + 2 * rows * 1536 * 2
+    d4 = moe.make_dims(64, 4096, 288, 1536, fmt="int4")
+    assert moe.moe_workspace_size(d4) < big  # one fp16 plane of h instead of two
+    for bad in (moe.make_dims(8, 200, 288, 64), moe.make_dims(8, 256, 288, 96),
+                moe.make_dims(8, 256, 600, 64), moe.make_dims(8, 256, 288, 64, top_k=17),
+                moe.make_dims(-1, 256, 288, 64), moe.make_dims(8, 256, 288, 64, I_shared=128),
+                moe.make_dims(8, 256, 4, 64, top_k=8), moe.make_dims(8, 256, 288, 64, fmt=7)):
+        assert moe.moe_workspace_size(bad) == 0
+
+
+class _Fake:
+    """Stands in for a tensor: an address and a byte size, never dereferenced."""
+
+    def __init__(self, addr, nbytes=0):
+        self.addr, self.nbytes = addr, nbytes
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def _call_forward(dims, ws_bytes, out_addr=0x10000, x_addr=0x20000):
+    w = moe.MoeWeights(0x30000, 0x40000, 0x50000, None, None, None)
+    return moe.lib().moe_ffn_forward(ctypes.byref(dims), x_addr, 0x60000, 0x70000,
+                                     ctypes.byref(w), ctypes.byref(w), out_addr, 0x80000,
+                                     ws_bytes, None)
+
+
+def test_argument_errors_before_any_launch(L):
+    d = moe.make_dims(8, 256, 288, 64)
+    need = moe.moe_workspace_size(d)
+    assert _call_forward(d, need, out_addr=0) == moe.MOE_ERR_INVALID_ARG
+    assert _call_forward(d, need, x_addr=0x20001) == moe.MOE_ERR_INVALID_ARG  # misaligned
+    assert _call_forward(d, need - 1) == moe.MOE_ERR_WORKSPACE
+    bad = moe.make_dims(8, 200, 288, 64)
+    assert _call_forward(bad, need) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_ffn_forward(None, 0, 0, 0, None, None, 0, 0, 0, None) == moe.MOE_ERR_INVALID_ARG
+    # Int4 weights need their scale pointers
+    d4 = moe.make_dims(8, 256, 288, 64, fmt="int4")
+    assert _call_forward(d4, moe.moe_workspace_size(d4)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_zero_tokens_is_a_no_op(L):
+    d = moe.make_dims(0, 256, 288, 64)
+    assert L.moe_ffn_forward(ctypes.byref(d), None, None, None, None, None, None, None, 0,
+                             None) == moe.MOE_OK
+
+
+def test_valid_call_without_gpu_fails_loudly(L):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    d = moe.make_dims(8, 256, 288, 64)
+    rc = _call_forward(d, moe.moe_workspace_size(d))
+    assert rc in (moe.MOE_ERR_CUDA, moe.MOE_ERR_UNSUPPORTED)
+    with pytest.raises(moe.MoeError):
+        moe.moe_combine(d, _Fake(0x1000), _Fake(0x2000), _Fake(0x3000), _Fake(0x4000), stream=0)
+
+
+def test_missing_library_raises(tmp_path, monkeypatch):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.lib()
