@@ -203,6 +203,37 @@ moe_status moe_workspace_status(void* ws, moe_stream_t stream);
  */
 moe_status moe_debug_wait_timeout(void* ws, uint64_t budget_ns, moe_stream_t stream);
 
+/*
+ * Router + top-k for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for the
+ * library's users.  Some callers cannot hand the library a workspace: a
+ * plugin or operator interface that passes only input and output pointers,
+ * code that must not call cudaMalloc while other work is in flight (the call
+ * synchronises the device), or a runtime that owns all device memory through
+ * its own pool and gives none out.  This variant takes only inputs and
+ * outputs.  Its scratch (the [T][E] fp32 router logits) lives in a
+ * fixed-size array inside the library, MOE_STATIC_ROUTER_LOGITS floats
+ * (1 MiB), which every GPU that loads the library keeps until the process
+ * exits.
+ *
+ * Arguments and results are those of moe_router_topk (same x, w_router,
+ * b_router, topk_idx, topk_w), except that the logits are always computed on
+ * the CUDA cores.  T * E above MOE_STATIC_ROUTER_LOGITS returns
+ * MOE_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array: calls that may overlap on the GPU (on
+ * different streams, or from different threads, without ordering between
+ * them) race on it and must be serialised by the caller.  The library
+ * allocates nothing in this call.
+ */
+#define MOE_STATIC_ROUTER_LOGITS (1u << 18)
+moe_status moe_router_topk_static_scratch(const moe_dims* d, const void* x, const void* w_router,
+                                          const float* b_router, int32_t* topk_idx,
+                                          float* topk_w, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,11 @@ FMT = {"bf16": MOE_W_BF16, "int4": MOE_W_INT4_G32}
 # every symbol include/moe_ffn.h declares
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_size", "moe_router_topk",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
-           "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout")
+           "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout",
+           "moe_router_topk_static_scratch")
+
+# T * E limit of moe_router_topk_static_scratch (floats of its fixed scratch)
+MOE_STATIC_ROUTER_LOGITS = 1 << 18
 
 MOE_STAGE_COUNT = 4
 STAGE_NAMES = ("router_topk", "permute", "gateup_swiglu", "down_scatter")
@@ -89,6 +93,7 @@ def lib() -> ctypes.CDLL:
                                            ctypes.POINTER(MoeStageEvents), vp], i32),
                 "moe_workspace_status": ([vp, vp], i32),
                 "moe_debug_wait_timeout": ([vp, u64, vp], i32),
+                "moe_router_topk_static_scratch": ([pd, vp, vp, vp, vp, vp, vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -188,3 +193,15 @@ def moe_workspace_status(ws, stream=None) -> int:
 def moe_debug_wait_timeout(ws, budget_ns: int, stream=None):
     _check(lib().moe_debug_wait_timeout(_ptr(ws), int(budget_ns), _stream(stream)),
            "moe_debug_wait_timeout")
+
+
+def moe_router_topk_static_scratch(dims, x, w_router, b_router, topk_idx, topk_w, stream=None):
+    """moe_router_topk for callers that cannot allocate: no workspace argument.
+
+    The logits scratch is the library's own fixed array (T * E at most
+    MOE_STATIC_ROUTER_LOGITS); calls that overlap on the GPU race on it.
+    """
+    _check(lib().moe_router_topk_static_scratch(ctypes.byref(dims), _ptr(x), _ptr(w_router),
+                                                _ptr(b_router), _ptr(topk_idx), _ptr(topk_w),
+                                                _stream(stream)),
+           "moe_router_topk_static_scratch")

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/moe_ffn.h"
 #include "moe_kernels.h"
 #include "ptx.cuh"
@@ -477,3 +479,63 @@ moe_status moe_debug_wait_timeout(void* ws, uint64_t budget_ns, moe_stream_t str
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Router + top-k without a caller workspace.
+//
+// For callers that cannot allocate device memory (an operator interface that
+// passes only inputs and outputs, a loop that must not synchronise the device
+// through cudaMalloc, a runtime whose pool gives nothing out), the router
+// logits live in this fixed array instead of the workspace.  It is part of
+// the library's device image, so every GPU that loads the library holds it
+// (1 MiB) until the process exits.  All calls share it; overlapping calls
+// race.  The logits are rewritten in full by every call before the top-k
+// kernel reads them, so nothing in it needs clearing between calls.
+static __device__ __align__(256) float g_static_router_logits[MOE_STATIC_ROUTER_LOGITS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+float* g_static_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_static_router_logits on the current device, looked up
+// once per device (host code only sees a host-side stand-in for the symbol).
+moe_status static_scratch_for_current_device(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_router_logits) != cudaSuccess || !p)
+      return MOE_ERR_CUDA;
+    g_static_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_router_topk_static_scratch(const moe_dims* d, const void* x,
+                                                     const void* w_router, const float* b_router,
+                                                     int32_t* topk_idx, float* topk_w,
+                                                     moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!x || !w_router || !b_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<uint64_t>(d->T) * static_cast<uint64_t>(d->E) > MOE_STATIC_ROUTER_LOGITS)
+    return MOE_ERR_WORKSPACE;
+  if ((st = check_device()) != MOE_OK) return st;
+  float* z = nullptr;
+  if ((st = static_scratch_for_current_device(&z)) != MOE_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_router_logits_simt(static_cast<const uint16_t*>(x),
+                                static_cast<const uint16_t*>(w_router), b_router, z, d->T, d->H,
+                                d->E, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return from_cuda(launch_topk(z, d->T, d->E, d->top_k, topk_idx, topk_w, s));
+}
