@@ -89,6 +89,24 @@ def gateup_bytes(wl, distinct):
     return w + rows * wl.H * 2 + h
 
 
+def gateup_traffic_per_launch(wl, units):
+    """DRAM bytes of one gate/up launch from the committed ncu capture
+    (profiles/gateup_traffic.json), scaled by the expert units processed;
+    None when the kernel source changed since the capture or the workload
+    shape differs."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+    if not os.path.exists(p) or wl.fmt != "bf16" or (wl.H, wl.I) != (4096, 1536):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if not sha.startswith(rec["source_sha256_prefix"]):
+        return None
+    return rec["dram_bytes_per_unit"] * units
+
+
 def flops_per_token(wl):
     return 2 * wl.E * wl.H + (wl.top_k + 1) * 2 * 3 * wl.H * wl.I
 
@@ -107,7 +125,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -166,11 +184,13 @@ def oracle_sample(wl, x, w_router, b_router, experts, shared, budget_s=12.0):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="decode_bf16", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the routed expert count (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
@@ -290,6 +310,7 @@ def run_ours(args, wl, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start before the timed steps
         for s in range(args.steps):
             flush.zero_()
             moe.moe_ffn_forward_timed(dims, xs[s % N_BATCHES], wr, b, exw, shw, out, ws,
@@ -364,7 +385,8 @@ def run_ours(args, wl, rank, world, local):
             "config": config_of(wl, world),
             "roofline": {"bound": "hbm", "kernel": "gateup_swiglu (tcgen05 grouped gate/up)",
                          "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak,
+                         "traffic": gateup_traffic_per_launch(wl, mean_distinct + 1),
                          "peak_source": f"{peak_src} hbm_gbs",
                          "algorithmic_bytes_per_launch": gu_bytes, "mean_launch_ms": gu_ms},
             "layer": {"algorithmic_GBps": layer_gbs, "hbm_frac": layer_gbs / hbm_peak,
@@ -387,6 +409,9 @@ def main():
     args = parse()
     rank, world, local = dist_env()
     wl = synthetic.WORKLOADS[args.workload].with_tokens(args.tokens)
+    if args.experts:
+        from dataclasses import replace
+        wl = replace(wl, E=args.experts)
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
     else:
