@@ -77,6 +77,9 @@ moe_status check_dims(const moe_dims* d) {
   if (d->I % 64 != 0 || d->I_shared != d->I) return MOE_ERR_UNSUPPORTED;
   if (d->E > kMaxE || d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->T) * (d->top_k + 1) > (1 << 30)) return MOE_ERR_UNSUPPORTED;
+  // Int4: a raw stage covers 256 reduction elements and the scale rows
+  // (K/32 bf16) must be a whole number of 16-byte TMA strides
+  if (d->fmt == MOE_W_INT4_G32 && (d->H % 256 != 0 || d->I % 256 != 0)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -151,6 +154,34 @@ bool encode_weights(CUtensorMap* m, const void* base, bool bf16, uint64_t K, uin
             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Codes of an Int4 stack [n][N][K/2] bytes: box {128 bytes, 128 rows, 1},
+// 128-byte swizzle (the dequantisers read 16-byte chunks conflict-free).
+bool encode_codes(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t n_experts) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {K / 2, N, n_experts};
+  const cuuint64_t strides[2] = {K / 2, K / 2 * N};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scales of an Int4 stack [n][N][K/32] bf16: box {8 groups, 128 rows, 1}
+// (256 reduction elements), no swizzle.
+bool encode_scales(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t n_experts) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {K / 32, N, n_experts};
+  const cuuint64_t strides[2] = {K / 32 * 2, K / 32 * 2 * N};
+  const cuuint32_t box[3] = {8, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool weights_ok(const moe_weights* w, int fmt) {
@@ -247,11 +278,70 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
                        const moe_weights* ex, const moe_weights* sh, int epilogue,
                        const int32_t* gather, const float* roww, float* out, const Ws& ws,
                        cudaStream_t s, const moe_stage_events* ev = nullptr) {
-  if (d.fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;  // Int4 grouped GEMM: see below
   const int rows = rows_of(d);
   const int BN = pick_bn(d.T);
   const int nsm = sm_count();
   const int max_entries = (d.E + 1) + (rows + BN - 1) / BN;
+  if (d.fmt == MOE_W_INT4_G32) {
+    Int4Launch G{};
+    if (!encode_codes(&G.tm_c[0], ex->gate, d.H, d.I, d.E) ||
+        !encode_codes(&G.tm_c[1], ex->up, d.H, d.I, d.E) ||
+        !encode_scales(&G.tm_s[0], ex->gate_scale, d.H, d.I, d.E) ||
+        !encode_scales(&G.tm_s[1], ex->up_scale, d.H, d.I, d.E) ||
+        !encode_codes(&G.tm_sc[0], sh->gate, d.H, d.I, 1) ||
+        !encode_codes(&G.tm_sc[1], sh->up, d.H, d.I, 1) ||
+        !encode_scales(&G.tm_ss[0], sh->gate_scale, d.H, d.I, 1) ||
+        !encode_scales(&G.tm_ss[1], sh->up_scale, d.H, d.I, 1) ||
+        !encode_kmajor(&G.tm_b, x_perm, false, d.H, rows, 1, 16))
+      return MOE_ERR_CUDA;
+    G.table = table;
+    G.BN = BN;
+    G.na = 2;
+    G.K = d.H;
+    G.N_out = d.I;
+    G.mblocks = d.I / 128;
+    G.E = d.E;
+    G.total_rows = rows;
+    G.out_rows = d.T;
+    G.epilogue = kEpiStoreRows;
+    G.h = ws.at<void>(ws.L.h0);
+    G.status = ws.status();
+    G.budget_ns = kWaitBudgetNs;
+    G.grid = max_entries * G.mblocks < nsm ? max_entries * G.mblocks : nsm;
+    record(ev, 2, s);
+    if (launch_int4_gemm(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(ev, 3, s);
+    Int4Launch D{};
+    if (!encode_codes(&D.tm_c[0], ex->down, d.I, d.H, d.E) ||
+        !encode_scales(&D.tm_s[0], ex->down_scale, d.I, d.H, d.E) ||
+        !encode_codes(&D.tm_sc[0], sh->down, d.I, d.H, 1) ||
+        !encode_scales(&D.tm_ss[0], sh->down_scale, d.I, d.H, 1) ||
+        !encode_kmajor(&D.tm_b, G.h, false, d.I, rows, 1, 16))
+      return MOE_ERR_CUDA;
+    D.tm_c[1] = D.tm_c[0];
+    D.tm_s[1] = D.tm_s[0];
+    D.tm_sc[1] = D.tm_sc[0];
+    D.tm_ss[1] = D.tm_ss[0];
+    D.table = table;
+    D.BN = BN;
+    D.na = 1;
+    D.K = d.I;
+    D.N_out = d.H;
+    D.mblocks = d.H / 128;
+    D.E = d.E;
+    D.total_rows = rows;
+    D.out_rows = d.T;
+    D.epilogue = epilogue;
+    D.gather = gather;
+    D.roww = roww;
+    D.out = out;
+    D.status = ws.status();
+    D.budget_ns = kWaitBudgetNs;
+    D.grid = max_entries * D.mblocks < nsm ? max_entries * D.mblocks : nsm;
+    const cudaError_t e = launch_int4_gemm(D, s);
+    record(ev, 4, s);
+    return from_cuda(e);
+  }
 
   GateUpLaunch G{};
   const bool bf16 = true;
@@ -329,7 +419,6 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   Ws w;
   if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
   if ((st = check_device()) != MOE_OK) return st;
-  if (d->fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Layout& L = w.L;
   record(ev, 0, s);
@@ -417,7 +506,6 @@ moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* 
   Ws w;
   if ((st = check_ws(*d, ws, ws_bytes, &w)) != MOE_OK) return st;
   if ((st = check_device()) != MOE_OK) return st;
-  if (d->fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t* table = w.at<int32_t>(w.L.table);
   const int capacity =

@@ -1,0 +1,461 @@
+// Grouped expert GEMMs over grouped-Int4 weights: in-kernel dequantisation
+// into fp16 tensor-core operands (tcgen05 kind::f16, fp32 accumulation).
+//
+// Weights use the grouped fmt=4 Int4 format decoded as offset-binary,
+// value = (nibble - 8) * scale ("feat(glm53): add device-resident HIP backend
+// for MI350P", section "Key changes"), with one bf16 scale per 32 reduction
+// elements.  (nibble - 8) * scale is exact in fp16 for every scale that fp16
+// represents (a 4-bit integer times an 8-bit significand fits fp16's 11), so
+// the fp16 operand equals the decoded weight and the only rounding left is
+// the fp32 accumulation.  Activations arrive as fp16 (x rows converted
+// exactly from bf16 by the permutation; h written as fp16 by gate/up).
+//
+// CTA = 11 warps, persistent over the same flat tile list as the bf16 path:
+//   warp 0, lane 0   raw producer: TMA of packed codes (128-byte swizzle) and
+//                    scales for 256 reduction elements per raw stage
+//   warp 1           TMEM allocation; lane 0 issues tcgen05.mma
+//   warps 2..5       epilogue (TMEM quadrant reads)
+//   warps 6..9       dequantisers: thread r owns weight row r of the tile; per
+//                    64-element sub-block it turns 8 code words per matrix
+//                    into 8 fp16 16-byte chunks, written straight into the
+//                    128-byte-swizzled operand layout the MMA reads
+//   warp 10, lane 0  activation producer: TMA of the token rows (fp16)
+// Operand slots carry two barriers, one for the activation bytes (TMA) and
+// one for the 128 dequantiser arrivals, so that after an abort every copy
+// still in flight can be waited for on its own barrier.
+#include <cuda_fp16.h>
+
+#include "moe_kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                        // K per operand slot (one swizzle row of fp16)
+constexpr int kRawK = 256;                     // K per raw stage
+constexpr int kSubPerRaw = kRawK / kBK;        // 4
+constexpr int kRowBytes = kBK * 2;             // 128
+constexpr int kChunkRows = 16;
+constexpr int kChunkBytes = kChunkRows * kRowBytes;
+constexpr int kATileBytes = kBM * kRowBytes;   // 16 KB fp16 operand
+constexpr int kCodeTileBytes = kBM * (kRawK / 2);  // 16 KB packed codes
+constexpr int kScaleTileBytes = kBM * (kRawK / 32) * 2;  // 2 KB bf16 scales
+constexpr int kBudget = 224 * 1024;
+constexpr int kThreads = 352;
+constexpr int kDqThread0 = 192;                // first dequantiser thread
+constexpr int kBWarp = 10;
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int ceil_pow2_32(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int BN, int NA>
+struct Int4Cfg {
+  static constexpr int kSlotBytes = NA * kATileBytes + BN * kRowBytes;
+  static constexpr int kRawBytes = NA * (kCodeTileBytes + kScaleTileBytes);
+  static constexpr int kRaw = NA == 2 ? 2 : 4;
+  static constexpr int kSlots = cmin(NA == 2 ? 4 : 6, (kBudget - kRaw * kRawBytes) / kSlotBytes);
+  static constexpr int kAccStages = (2 * NA * BN <= 512) ? 2 : 1;
+  static constexpr int kAccCols = NA * BN;
+  static constexpr int kTmemCols = ceil_pow2_32(kAccStages * kAccCols);
+  static constexpr int kSmemBytes = kSlots * kSlotBytes + kRaw * kRawBytes + 1024 + 512;
+  static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte alignment");
+  static_assert(kSlots >= 2, "at least two operand slots");
+};
+
+struct Int4Args {
+  const int32_t* table;
+  int K, N_out, mblocks, E, total_rows, out_rows;
+  const int32_t* gather;
+  const float* roww;
+  float* out;      // down: scatter-add [T][N_out] or rows [rows][N_out]
+  __half* h;       // gate/up: h [rows][N_out]
+  int* status;
+  uint64_t budget_ns;
+};
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+__device__ __forceinline__ float clamped_swiglu(float g, float u) {
+  const float gc = fminf(g, 10.0f);
+  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
+  return gc / (1.0f + expf(-gc)) * uc;
+}
+
+// Eight consecutive codes of one 32-bit word (element 2m in the low nibble of
+// byte m) -> eight fp16 weights (code - 8) * s, as one 16-byte chunk.
+// 0x6400 | n is the fp16 value 1024 + n; subtracting 1032 leaves n - 8 exactly.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t p0 = (__byte_perm(lo, hi, 0x0400) & 0x00FF00FFu) | 0x64006400u;
+  const uint32_t p1 = (__byte_perm(lo, hi, 0x0501) & 0x00FF00FFu) | 0x64006400u;
+  const uint32_t p2 = (__byte_perm(lo, hi, 0x0602) & 0x00FF00FFu) | 0x64006400u;
+  const uint32_t p3 = (__byte_perm(lo, hi, 0x0703) & 0x00FF00FFu) | 0x64006400u;
+  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  uint32_t r[4];
+  const uint32_t p[4] = {p0, p1, p2, p3};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), off);
+    v = __hmul2(v, s2);
+    r[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ __half bf16_bits_to_half(uint32_t bits16) {
+  return __float2half_rn(__uint_as_float(bits16 << 16));
+}
+
+__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int i) {
+  const int4 v =
+      reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + kTableHeaderBytes)[i];
+  return TileEntry{v.x, v.y, v.z, v.w};
+}
+
+template <int BN, int NA, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    int4_gemm_kernel(const __grid_constant__ CUtensorMap tm_c0,
+                     const __grid_constant__ CUtensorMap tm_c1,
+                     const __grid_constant__ CUtensorMap tm_s0,
+                     const __grid_constant__ CUtensorMap tm_s1,
+                     const __grid_constant__ CUtensorMap tm_sc0,
+                     const __grid_constant__ CUtensorMap tm_sc1,
+                     const __grid_constant__ CUtensorMap tm_ss0,
+                     const __grid_constant__ CUtensorMap tm_ss1,
+                     const __grid_constant__ CUtensorMap tm_b, const Int4Args a) {
+  using Cfg = Int4Cfg<BN, NA>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* slots = base;
+  uint8_t* raws = base + Cfg::kSlots * Cfg::kSlotBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raws + Cfg::kRaw * Cfg::kRawBytes);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + Cfg::kRaw;
+  uint64_t* b_full = raw_empty + Cfg::kRaw;
+  uint64_t* a_full = b_full + Cfg::kSlots;
+  uint64_t* op_empty = a_full + Cfg::kSlots;
+  uint64_t* tfull = op_empty + Cfg::kSlots;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::kRaw; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], 128);
+    }
+    for (int i = 0; i < Cfg::kSlots; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&a_full[i], 128);
+      mbar_init(&op_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const AbortState ab{abort_flag, a.status, a.budget_ns};
+
+  pdl_wait();
+  pdl_launch_dependents();
+  const int total = a.table[0] * a.mblocks;
+  const int KB = a.K / kBK;                       // operand slots per tile
+  const int RB = (a.K + kRawK - 1) / kRawK;       // raw stages per tile
+
+  auto code_tile = [&](int rs, int m) { return raws + rs * Cfg::kRawBytes + m * kCodeTileBytes; };
+  auto scale_tile = [&](int rs, int m) {
+    return raws + rs * Cfg::kRawBytes + NA * kCodeTileBytes + m * kScaleTileBytes;
+  };
+  auto a_tile = [&](int os, int m) { return slots + os * Cfg::kSlotBytes + m * kATileBytes; };
+  auto b_tile = [&](int os) { return slots + os * Cfg::kSlotBytes + NA * kATileBytes; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- raw producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int rs = 0;
+      uint32_t rph = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const int mb = tile % a.mblocks;
+        const bool sh = te.group == a.E;
+        const int ge = sh ? 0 : te.group;
+        for (int rb = 0; rb < RB; ++rb) {
+          if (!mbar_wait(&raw_empty[rs], rph ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[rs], Cfg::kRawBytes);
+          armed |= 1u << rs;
+          armed_par = (armed_par & ~(1u << rs)) | (rph << rs);
+          tma_load_3d(code_tile(rs, 0), sh ? &tm_sc0 : &tm_c0, &raw_full[rs], rb * (kRawK / 2),
+                      mb * kBM, ge, pol);
+          tma_load_3d(scale_tile(rs, 0), sh ? &tm_ss0 : &tm_s0, &raw_full[rs], rb * (kRawK / 32),
+                      mb * kBM, ge, pol);
+          if (NA == 2) {
+            tma_load_3d(code_tile(rs, 1), sh ? &tm_sc1 : &tm_c1, &raw_full[rs], rb * (kRawK / 2),
+                        mb * kBM, ge, pol);
+            tma_load_3d(scale_tile(rs, 1), sh ? &tm_ss1 : &tm_s1, &raw_full[rs],
+                        rb * (kRawK / 32), mb * kBM, ge, pol);
+          }
+          if (++rs == Cfg::kRaw) {
+            rs = 0;
+            rph ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < Cfg::kRaw; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&raw_full[s], (armed_par >> s) & 1u);
+    }
+  } else if (warp == kBWarp) {
+    // ---------------------------------------------------------------- activation producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      int os = 0;
+      uint32_t oph = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&b_full[os], nchunks * kChunkBytes);
+          armed |= 1u << os;
+          armed_par = (armed_par & ~(1u << os)) | (oph << os);
+          for (int c = 0; c < nchunks; ++c)
+            tma_load_2d(b_tile(os) + c * kChunkBytes, &tm_b, &b_full[os], kb * kBK,
+                        te.row0 + c * kChunkRows, pol);
+          if (++os == Cfg::kSlots) {
+            os = 0;
+            oph ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < Cfg::kSlots; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&b_full[s], (armed_par >> s) & 1u);
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- dequantisers
+    const int r = threadIdx.x - kDqThread0;  // weight row of the tile
+    const int sw = r & 7;                    // 128-byte swizzle phase of this row
+    int rs = 0, os = 0;
+    uint32_t rph = 0, oph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int rb = 0; ok && rb < RB; ++rb) {
+        if (!mbar_wait(&raw_full[rs], rph, ab)) {
+          ok = false;
+          break;
+        }
+        uint4 sv[NA];
+#pragma unroll
+        for (int m = 0; m < NA; ++m)
+          sv[m] = *reinterpret_cast<const uint4*>(scale_tile(rs, m) + r * 16);
+        const int nsub = cmin(kSubPerRaw, KB - rb * kSubPerRaw);
+        for (int sb = 0; sb < nsub; ++sb) {
+          if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int m = 0; m < NA; ++m) {
+            const uint32_t sw4[4] = {sv[m].x, sv[m].y, sv[m].z, sv[m].w};
+            uint8_t* at = a_tile(os, m) + r * kRowBytes;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int j = sb * 2 + half;     // 16-byte code chunk = 32 elements = one group
+              const uint32_t sbits = (sw4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+              const __half s = bf16_bits_to_half(sbits);
+              const __half2 s2 = __halves2half2(s, s);
+              const uint4 cw = *reinterpret_cast<const uint4*>(code_tile(rs, m) + r * 128 +
+                                                               ((j ^ sw) << 4));
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int wd = 0; wd < 4; ++wd) {
+                const int c_out = half * 4 + wd;
+                *reinterpret_cast<uint4*>(at + ((c_out ^ sw) << 4)) = dequant8(words[wd], s2);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&a_full[os]);
+          if (++os == Cfg::kSlots) {
+            os = 0;
+            oph ^= 1u;
+          }
+        }
+        mbar_arrive(&raw_empty[rs]);
+        if (++rs == Cfg::kRaw) {
+          rs = 0;
+          rph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_f16(kBM, 16, false) & ~(0x3Fu << 17);
+      int os = 0, acc = 0;
+      uint32_t oph = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ab)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + acc * Cfg::kAccCols;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&b_full[os], oph, ab) || !mbar_wait(&a_full[os], oph, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(os)));
+          const uint64_t da0 = sw128_kmajor_desc(smem_u32(a_tile(os, 0)));
+          const uint64_t da1 = sw128_kmajor_desc(smem_u32(a_tile(os, NA - 1)));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t accum = (kb | k) != 0;
+            umma_f16(d0, da0 + 2 * k, db + 2 * k, idesc, accum);
+            if (NA == 2) umma_f16(d0 + BN, da1 + 2 * k, db + 2 * k, idesc, accum);
+          }
+          umma_commit(&op_empty[os]);
+          if (++os == Cfg::kSlots) {
+            os = 0;
+            oph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (Cfg::kAccStages == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileEntry te = entry_at(a.table, tile / a.mblocks);
+      const int mb = tile % a.mblocks;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
+      tc_fence_after_sync();
+      const int f = mb * kBM + q * 32 + lane;
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
+      const int n = round16(te.nrows);
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        uint32_t v0[16], v1[16];
+        tmem_ld_32x32b_x16(tq + c0, v0);
+        if (NA == 2) tmem_ld_32x32b_x16(tq + BN + c0, v1);
+        tmem_ld_wait();
+        if (f < a.N_out) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            const int rr = te.row0 + c;
+            if (c < te.nrows && rr < a.total_rows) {
+              const float d = __uint_as_float(v0[i]);
+              if (NA == 2) {
+                const float hv = clamped_swiglu(d, __uint_as_float(v1[i]));
+                a.h[static_cast<size_t>(rr) * a.N_out + f] = __float2half_rn(hv);
+              } else if (EPI == kEpiScatterAdd) {
+                const int t = a.gather[rr];
+                if (t >= 0 && t < a.out_rows)
+                  atomicAdd(a.out + static_cast<size_t>(t) * a.N_out + f, a.roww[rr] * d);
+              } else {
+                a.out[static_cast<size_t>(rr) * a.N_out + f] = d;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tempty[acc]);
+      if (Cfg::kAccStages == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <int BN, int NA, int EPI>
+cudaError_t int4_dispatch(const Int4Launch& L, cudaStream_t s) {
+  using Cfg = Int4Cfg<BN, NA>;
+  auto kern = int4_gemm_kernel<BN, NA, EPI>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  Int4Args a{L.table, L.K, L.N_out, L.mblocks, L.E, L.total_rows, L.out_rows,
+             L.gather, L.roww, L.out, static_cast<__half*>(L.h), L.status, L.budget_ns};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_c[0], L.tm_c[1], L.tm_s[0], L.tm_s[1], L.tm_sc[0],
+                            L.tm_sc[1], L.tm_ss[0], L.tm_ss[1], L.tm_b, a);
+}
+
+template <int NA, int EPI>
+cudaError_t int4_by_bn(const Int4Launch& L, cudaStream_t s) {
+  switch (L.BN) {
+    case 16: return int4_dispatch<16, NA, EPI>(L, s);
+    case 32: return int4_dispatch<32, NA, EPI>(L, s);
+    case 64: return int4_dispatch<64, NA, EPI>(L, s);
+    case 128: return int4_dispatch<128, NA, EPI>(L, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s) {
+  if (L.na == 2) return int4_by_bn<2, kEpiStoreRows>(L, s);
+  if (L.epilogue == kEpiScatterAdd) return int4_by_bn<1, kEpiScatterAdd>(L, s);
+  return int4_by_bn<1, kEpiStoreRows>(L, s);
+}
+
+}  // namespace moe

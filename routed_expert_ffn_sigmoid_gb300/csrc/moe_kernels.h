@@ -102,6 +102,25 @@ struct DownLaunch {
 };
 cudaError_t launch_down(const DownLaunch& L, cudaStream_t s);
 
+// Grouped GEMM over grouped-Int4 weights (dequantised in-kernel to fp16).
+// na = 2: gate/up with the clamped SwiGLU, h written as fp16 [rows][N_out];
+// na = 1: down with the scatter-add or store-rows epilogue.
+struct Int4Launch {
+  CUtensorMap tm_c[2], tm_s[2];    // codes / scales of the routed stacks
+  CUtensorMap tm_sc[2], tm_ss[2];  // codes / scales of the shared expert
+  CUtensorMap tm_b;                // fp16 activation rows
+  const int32_t* table;
+  int BN, na, K, N_out, mblocks, E, total_rows, out_rows, epilogue;
+  const int32_t* gather;
+  const float* roww;
+  float* out;
+  void* h;
+  int* status;
+  uint64_t budget_ns;
+  int grid;
+};
+cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
+
 // Diagnostic bounded wait on a barrier nothing completes.
 cudaError_t launch_wait_selftest(int* status, uint64_t budget_ns, cudaStream_t s);
 

@@ -84,9 +84,18 @@ class DeviceLayer:
         return idx.cpu().numpy(), w.cpu().numpy()
 
 
+# Routing-weight tolerance.  w_j = s_j / sum s with s = sigmoid(z), so a logit
+# error dz moves ln w_j by at most 2 max|dz|.  Both sides accumulate the logit
+# in fp32 over H = 4096 products, in different orders (the tensor-core router
+# adds in a tree); the tree's bound is ~log2(H) * 2^-24 * sum|x_h w_h| with
+# sum|x_h w_h| ~ H * E|x| * E|w| = 4096 * 0.8 * 0.016 = 52, i.e. |dz| <~ 4e-5,
+# hence a relative weight tolerance of 1e-4.
+W_REL_TOL = 1e-4
+
+
 def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, z_ref):
     """Expert sets bit-exact; slot order where the oracle's adjacent logits
-    differ by more than 1e-4; weights per expert id within 1e-5 relative."""
+    differ by more than 1e-4; weights per expert id within W_REL_TOL."""
     T, k = idx_ref.shape
     for t in range(T):
         assert sorted(idx_gpu[t].tolist()) == sorted(idx_ref[t].tolist()), f"token {t}"
@@ -99,4 +108,5 @@ def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, z_ref):
         ref_by_e = dict(zip(idx_ref[t].tolist(), w_ref[t].tolist()))
         for j in range(k):
             e = int(idx_gpu[t, j])
-            assert abs(w_gpu[t, j] - ref_by_e[e]) <= 1e-5 * ref_by_e[e] + 1e-7, f"token {t} e {e}"
+            assert abs(w_gpu[t, j] - ref_by_e[e]) <= W_REL_TOL * ref_by_e[e] + 1e-7, \
+                f"token {t} e {e}: {w_gpu[t, j]} vs {ref_by_e[e]}"

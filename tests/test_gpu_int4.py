@@ -1,0 +1,140 @@
+"""GPU parity of the grouped-Int4 path (offset-binary nibble - 8, bf16 scale
+per 32 elements) with the CPU oracle: max|err| / RMS(oracle) <= 5e-3."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from moe_inputs import gapped_x, make_inputs, rel_max_err
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import routed_expert_ffn_sigmoid_gb300 as moe  # noqa: E402
+from gpu_helpers import TOL, DeviceLayer, compare_routing, dev_u16  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def small4():
+    wl = synthetic.Workload("small_int4", 24, 256, 16, 256, 256, 8, "int4", 40, tokens=(24,))
+    return DeviceLayer(make_inputs(wl))
+
+
+@pytest.fixture(scope="module")
+def decode4():
+    return DeviceLayer(make_inputs(synthetic.WORKLOADS["decode_int4"]))
+
+
+@pytest.fixture(scope="module")
+def skewed4():
+    return DeviceLayer(make_inputs(synthetic.WORKLOADS["skewed_prefill_int4"]))
+
+
+def _ref(layer, x):
+    inp = layer.inp
+    out, _, _ = oracle.moe_forward(x, inp.w_router, inp.b_router, inp.experts, inp.shared, "int4")
+    return out
+
+
+def test_forward_small_int4(small4):
+    out = small4.forward(small4.inp.x)
+    assert rel_max_err(out, _ref(small4, small4.inp.x)) <= TOL["int4"]
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_forward_decode_int4(decode4, T):
+    x = decode4.inp.x[:T]
+    out = decode4.forward(x)
+    assert rel_max_err(out, _ref(decode4, x)) <= TOL["int4"]
+
+
+def test_permute_int4_converts_rows_to_fp16(decode4):
+    T = 64
+    x = decode4.inp.x[:T]
+    z = oracle.router_logits(x, decode4.inp.w_router, decode4.inp.b_router)
+    idx, _, _ = oracle.topk(z, 8)
+    dims = decode4.dims(T)
+    rows = 9 * T
+    ws = decode4.workspace(T)
+    off = torch.empty(decode4.wl.E + 2, dtype=torch.int32, device="cuda")
+    gather = torch.empty(rows, dtype=torch.int32, device="cuda")
+    row_of = torch.empty((T, 8), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((rows, decode4.wl.H), dtype=torch.float16, device="cuda")
+    moe.moe_permute(dims, torch.from_numpy(idx).cuda(), dev_u16(x), off, gather, row_of, x_perm, ws)
+    torch.cuda.synchronize()
+    r_off, r_gather, r_row_of = oracle.permute(idx, decode4.wl.E)
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    assert np.array_equal(gather.cpu().numpy(), r_gather)
+    want = synthetic.bf16_bits_to_f32(x[r_gather]).astype(np.float16)
+    assert np.array_equal(x_perm.cpu().numpy(), want)
+
+
+def test_expert_ffn_int4_rows(decode4):
+    T = 8
+    x = decode4.inp.x[:T]
+    z = oracle.router_logits(x, decode4.inp.w_router, decode4.inp.b_router)
+    idx, _, _ = oracle.topk(z, 8)
+    off, gather, row_of = oracle.permute(idx, decode4.wl.E)
+    rows = int(off[-1])
+    x_perm = torch.from_numpy(synthetic.bf16_bits_to_f32(x[gather]).astype(np.float16)).cuda()
+    y = torch.empty((rows, decode4.wl.H), dtype=torch.float32, device="cuda")
+    ws = decode4.workspace(T)
+    moe.moe_expert_ffn(decode4.dims(T), x_perm, torch.from_numpy(off).cuda(), decode4.exw,
+                       decode4.shw, y, ws)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    inp = decode4.inp
+    ref = oracle.expert_rows(x, off, gather, inp.experts, inp.shared, "int4", 0, rows)
+    assert rel_max_err(y.cpu().numpy(), ref) <= TOL["int4"]
+
+
+def test_forward_skewed_prefill_int4_sampled(skewed4):
+    x = skewed4.inp.x
+    idx, w = skewed4.router(x)
+    counts = np.bincount(idx.ravel(), minlength=skewed4.wl.E)
+    assert counts.max() > 8000 and (counts == 0).sum() > 100  # the load really is skewed
+    out = skewed4.forward(x)
+    assert np.all(np.isfinite(out))
+    rng = np.random.default_rng(4)
+    sample = np.unique(np.concatenate([rng.choice(x.shape[0], 40, replace=False),
+                                       [0, x.shape[0] - 1]]))
+    assert rel_max_err(out[sample], _ref(skewed4, x[sample])) <= TOL["int4"]
+
+
+def test_router_skewed_prefill(skewed4):
+    x = skewed4.inp.x[:2048]
+    idx, w = skewed4.router(x)
+    z = oracle.router_logits(x, skewed4.inp.w_router, skewed4.inp.b_router)
+    ridx, rw, _ = oracle.topk(z, 8)
+    compare_routing(idx, w, ridx, rw, z)
+
+
+def test_int4_rejects_unaligned_shapes(small4):
+    dims = moe.make_dims(8, 384, 16, 256, fmt="int4")  # H not a multiple of 256
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty((8, 384), dtype=torch.float32, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_ffn_forward(dims, dev_u16(np.zeros((8, 384), np.uint16)), small4.wr, small4.b,
+                            small4.exw, small4.shw, out, ws)
+    assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_forward_int4_forced_overflow(decode4):
+    T = 300
+    x, _, _ = gapped_x(decode4.wl, decode4.inp.w_router, decode4.inp.b_router, T=T)
+    forced = [1, 2, 3, 100, 150, 200, 250, 287]
+    b = np.full(decode4.wl.E, -60.0, np.float32)
+    b[forced] = 60.0
+    saved = decode4.b
+    try:
+        decode4.b = torch.from_numpy(b).cuda()
+        out = decode4.forward(x)
+    finally:
+        decode4.b = saved
+    inp = decode4.inp
+    sample = np.arange(0, T, 29)
+    ref, idx, _ = oracle.moe_forward(x[sample], inp.w_router, b, inp.experts, inp.shared, "int4")
+    assert rel_max_err(out[sample], ref) <= TOL["int4"]

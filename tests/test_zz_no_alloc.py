@@ -62,7 +62,7 @@ def test_static_scratch_router_matches_workspace_router_twice(router, T):
             ref_by_e = dict(zip(ref_i[t].tolist(), ref_w[t].tolist()))
             for j in range(wl.top_k):
                 e = int(got_i[t, j])
-                assert abs(got_w[t, j] - ref_by_e[e]) <= 1e-5 * ref_by_e[e] + 1e-7
+                assert abs(got_w[t, j] - ref_by_e[e]) <= 1e-4 * ref_by_e[e] + 1e-7
 
 
 def test_static_scratch_router_refuses_oversized_inputs(router):
