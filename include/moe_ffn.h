@@ -168,7 +168,8 @@ moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_route
 /*
  * Stage boundaries of moe_ffn_forward_timed: ev[i] is recorded on `stream`
  * before stage i, ev[MOE_STAGE_COUNT] after the last one.  Stages:
- *   0 router logits + top-k      1 permutation (count, scan, scatter, gather)
+ *   0 router logits + top-k (for T <= 128 the top-k runs in stage 1, fused
+ *     with the permutation)     1 permutation (count, scan, scatter, gather)
  *   2 grouped gate/up + SwiGLU   3 grouped down + weighted scatter-add
  * Each ev[i] is a cudaEvent_t created by the caller (NULL entries are skipped).
  */

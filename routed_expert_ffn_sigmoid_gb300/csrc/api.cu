@@ -215,8 +215,10 @@ moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes, Ws* out) {
 
 // ------------------------------------------------------------ stages
 
-moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
-                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
+// Router logits into the workspace (tensor cores from kRouterTcMinTokens
+// tokens, CUDA cores below).
+moe_status run_logits(const moe_dims& d, const void* x, const void* w_router, const float* b,
+                      const Ws& ws, cudaStream_t s) {
   float* z = ws.at<float>(ws.L.z);
   cudaError_t e;
   if (d.T >= kRouterTcMinTokens) {
@@ -250,13 +252,20 @@ moe_status run_router(const moe_dims& d, const void* x, const void* w_router, co
     e = launch_router_logits_simt(static_cast<const uint16_t*>(x),
                                   static_cast<const uint16_t*>(w_router), b, z, d.T, d.H, d.E, s);
   }
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return from_cuda(launch_topk(z, d.T, d.E, d.top_k, idx, w, s));
+  return from_cuda(e);
+}
+
+moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
+                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
+  const moe_status st = run_logits(d, x, w_router, b, ws, s);
+  if (st != MOE_OK) return st;
+  return from_cuda(launch_topk(ws.at<float>(ws.L.z), d.T, d.E, d.top_k, idx, w, s));
 }
 
 moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, const void* x,
                        int32_t* offsets, int32_t* gather, int32_t* row_of, float* roww,
-                       void* x_perm, int32_t* table, const Ws& ws, cudaStream_t s) {
+                       void* x_perm, int32_t* table, const Ws& ws, cudaStream_t s,
+                       float* zero_out = nullptr) {
   int32_t* blockcnt = ws.at<int32_t>(ws.L.blockcnt);
   cudaError_t e = launch_perm_count(idx, d.T, d.E, d.top_k, blockcnt, s);
   if (e == cudaSuccess)
@@ -265,7 +274,8 @@ moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, co
     e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
   if (e == cudaSuccess)
     e = launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(d), d.H, d.T,
-                           d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), s);
+                           d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
+                           zero_out ? static_cast<size_t>(d.T) * d.H : 0, s);
   return from_cuda(e);
 }
 
@@ -421,20 +431,32 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   if ((st = check_device()) != MOE_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Layout& L = w.L;
-  record(ev, 0, s);
-  if (cudaMemsetAsync(out, 0, static_cast<size_t>(d->T) * d->H * sizeof(float), s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   int32_t* idx = w.at<int32_t>(L.idx);
   float* wts = w.at<float>(L.w);
-  if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
-  record(ev, 1, s);
   int32_t* gather = w.at<int32_t>(L.gather);
   float* roww = w.at<float>(L.roww);
   int32_t* table = w.at<int32_t>(L.table);
   void* x_perm = w.at<void>(L.x_perm);
-  if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of),
-                        roww, x_perm, table, w, s)) != MOE_OK)
-    return st;
+  record(ev, 0, s);
+  if (d->T <= kSmallT) {
+    // decode sizes: logits, then one CTA for top-k + the whole permutation
+    if ((st = run_logits(*d, x, w_router, b_router, w, s)) != MOE_OK) return st;
+    record(ev, 1, s);
+    if (launch_route_small(w.at<float>(L.z), d->T, d->E, d->top_k, pick_bn(d->T), idx, wts,
+                           w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of), roww,
+                           table, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T,
+                           d->fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), out,
+                           static_cast<size_t>(d->T) * d->H, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
+    record(ev, 1, s);
+    if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather,
+                          w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, out)) != MOE_OK)
+      return st;
+  }
   return run_experts(*d, x_perm, table, experts, shared, kEpiScatterAdd, gather, roww, out, w, s,
                      ev);
 }

@@ -10,16 +10,19 @@
 // the fp32 accumulation.  Activations arrive as fp16 (x rows converted
 // exactly from bf16 by the permutation; h written as fp16 by gate/up).
 //
-// CTA = 11 warps, persistent over the same flat tile list as the bf16 path:
+// CTA = 15 warps, persistent over the same flat tile list as the bf16 path:
 //   warp 0, lane 0   raw producer: TMA of packed codes (128-byte swizzle) and
 //                    scales for 256 reduction elements per raw stage
 //   warp 1           TMEM allocation; lane 0 issues tcgen05.mma
 //   warps 2..5       epilogue (TMEM quadrant reads)
-//   warps 6..9       dequantisers: thread r owns weight row r of the tile; per
-//                    64-element sub-block it turns 8 code words per matrix
-//                    into 8 fp16 16-byte chunks, written straight into the
-//                    128-byte-swizzled operand layout the MMA reads
-//   warp 10, lane 0  activation producer: TMA of the token rows (fp16)
+//   warps 6..13      dequantisers, two threads per weight row of the tile (one
+//                    per matrix for gate/up, one per 32-element half for
+//                    down); each turns code words into fp16 16-byte chunks
+//                    written straight into the 128-byte-swizzled operand
+//                    layout the MMA reads
+//   warp 14, lane 0  activation producer: TMA of the token rows (fp16)
+// The raw ring is as deep as shared memory allows (its stages are what carry
+// the HBM bytes); two to four operand slots decouple dequantisation from MMA.
 // Operand slots carry two barriers, one for the activation bytes (TMA) and
 // one for the 128 dequantiser arrivals, so that after an abort every copy
 // still in flight can be waited for on its own barrier.
@@ -42,9 +45,11 @@ constexpr int kATileBytes = kBM * kRowBytes;   // 16 KB fp16 operand
 constexpr int kCodeTileBytes = kBM * (kRawK / 2);  // 16 KB packed codes
 constexpr int kScaleTileBytes = kBM * (kRawK / 32) * 2;  // 2 KB bf16 scales
 constexpr int kBudget = 224 * 1024;
-constexpr int kThreads = 352;
+constexpr int kThreads = 480;
 constexpr int kDqThread0 = 192;                // first dequantiser thread
-constexpr int kBWarp = 10;
+constexpr int kDqThreads = 256;
+constexpr int kDqWarpEnd = 14;                 // dequantiser warps are 6 .. 13
+constexpr int kBWarp = 14;
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int ceil_pow2_32(int v) {
@@ -57,14 +62,14 @@ template <int BN, int NA>
 struct Int4Cfg {
   static constexpr int kSlotBytes = NA * kATileBytes + BN * kRowBytes;
   static constexpr int kRawBytes = NA * (kCodeTileBytes + kScaleTileBytes);
-  static constexpr int kRaw = NA == 2 ? 2 : 4;
-  static constexpr int kSlots = cmin(NA == 2 ? 4 : 6, (kBudget - kRaw * kRawBytes) / kSlotBytes);
+  static constexpr int kRaw = cmin(NA == 2 ? 4 : 6, (kBudget - 2 * kSlotBytes) / kRawBytes);
+  static constexpr int kSlots = cmin(4, (kBudget - kRaw * kRawBytes) / kSlotBytes);
   static constexpr int kAccStages = (2 * NA * BN <= 512) ? 2 : 1;
   static constexpr int kAccCols = NA * BN;
   static constexpr int kTmemCols = ceil_pow2_32(kAccStages * kAccCols);
   static constexpr int kSmemBytes = kSlots * kSlotBytes + kRaw * kRawBytes + 1024 + 512;
   static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte alignment");
-  static_assert(kSlots >= 2, "at least two operand slots");
+  static_assert(kSlots >= 2 && kRaw >= 2, "at least two operand slots and raw stages");
 };
 
 struct Int4Args {
@@ -150,11 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kRaw; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], 128);
+      mbar_init(&raw_empty[i], kDqThreads);
     }
     for (int i = 0; i < Cfg::kSlots; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&a_full[i], 128);
+      mbar_init(&a_full[i], kDqThreads);
       mbar_init(&op_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -257,10 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < Cfg::kSlots; ++s)
         if ((armed >> s) & 1u) mbar_wait_drain(&b_full[s], (armed_par >> s) & 1u);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < kDqWarpEnd) {
     // ---------------------------------------------------------------- dequantisers
-    const int r = threadIdx.x - kDqThread0;  // weight row of the tile
+    const int d = threadIdx.x - kDqThread0;
+    const int r = d & (kBM - 1);             // weight row of the tile
+    const int part = d >> 7;                 // gate/up: matrix; down: 32-element half
     const int sw = r & 7;                    // 128-byte swizzle phase of this row
+    const int m = NA == 2 ? part : 0;
     int rs = 0, os = 0;
     uint32_t rph = 0, oph = 0;
     bool ok = true;
@@ -270,34 +278,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint4 sv[NA];
-#pragma unroll
-        for (int m = 0; m < NA; ++m)
-          sv[m] = *reinterpret_cast<const uint4*>(scale_tile(rs, m) + r * 16);
+        const uint4 sv = *reinterpret_cast<const uint4*>(scale_tile(rs, m) + r * 16);
+        const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
+        const uint8_t* ct = code_tile(rs, m) + r * 128;
         const int nsub = cmin(kSubPerRaw, KB - rb * kSubPerRaw);
         for (int sb = 0; sb < nsub; ++sb) {
           if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
             ok = false;
             break;
           }
+          uint8_t* at = a_tile(os, m) + r * kRowBytes;
 #pragma unroll
-          for (int m = 0; m < NA; ++m) {
-            const uint32_t sw4[4] = {sv[m].x, sv[m].y, sv[m].z, sv[m].w};
-            uint8_t* at = a_tile(os, m) + r * kRowBytes;
+          for (int hh = 0; hh < (NA == 2 ? 2 : 1); ++hh) {
+            const int half = NA == 2 ? hh : part;
+            const int j = sb * 2 + half;       // 16-byte code chunk = 32 elements = one group
+            const uint32_t sbits = (sw4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+            const __half s1 = bf16_bits_to_half(sbits);
+            const __half2 s2 = __halves2half2(s1, s1);
+            const uint4 cw = *reinterpret_cast<const uint4*>(ct + ((j ^ sw) << 4));
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int j = sb * 2 + half;     // 16-byte code chunk = 32 elements = one group
-              const uint32_t sbits = (sw4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-              const __half s = bf16_bits_to_half(sbits);
-              const __half2 s2 = __halves2half2(s, s);
-              const uint4 cw = *reinterpret_cast<const uint4*>(code_tile(rs, m) + r * 128 +
-                                                               ((j ^ sw) << 4));
-              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-              for (int wd = 0; wd < 4; ++wd) {
-                const int c_out = half * 4 + wd;
-                *reinterpret_cast<uint4*>(at + ((c_out ^ sw) << 4)) = dequant8(words[wd], s2);
-              }
+            for (int wd = 0; wd < 4; ++wd) {
+              const int c_out = half * 4 + wd;
+              *reinterpret_cast<uint4*>(at + ((c_out ^ sw) << 4)) = dequant8(words[wd], s2);
             }
           }
           fence_proxy_async_smem();

@@ -13,6 +13,8 @@ constexpr int kMaxE = 512;        // routed experts supported by router / permut
 constexpr int kMaxTopK = 16;
 constexpr int kPermTokBlock = 128; // tokens per counting-sort block
 constexpr int kTableHeaderBytes = 16;
+constexpr int kSmallT = 128;       // tokens handled by the one-CTA routing kernel
+constexpr int kSmallThreads = 512;
 
 // One grouped-GEMM work entry: rows [row0, row0 + nrows) of group `group`
 // (group == E is the shared expert).  nrows <= the launch's token tile BN.
@@ -42,9 +44,17 @@ cudaError_t launch_perm_scan(int32_t* blockcnt, int T, int E, int k, int32_t* of
 cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_t* blockbase,
                                 int T, int E, int k, int32_t* gather, int32_t* row_of,
                                 float* roww, cudaStream_t s);
-// x_perm[r] = x[gather[r]]; to_fp16 converts bf16 -> fp16 on the way.
+// x_perm[r] = x[gather[r]]; to_fp16 converts bf16 -> fp16 on the way.  When
+// zero_out is not null the kernel also zeroes zero_n floats there (a multiple
+// of 4, 16-byte aligned).
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
-                               bool to_fp16, uint16_t* x_perm, cudaStream_t s);
+                               bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
+                               cudaStream_t s);
+// T <= kSmallT: top-k, histogram, offsets, stable ranks, gather / row_of /
+// row weights and the tile table in one CTA.
+cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
+                               float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
+                               float* roww, int32_t* table, cudaStream_t s);
 // Tile table from existing offsets (for the unfused expert entry point);
 // at most `capacity` entries.
 cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,

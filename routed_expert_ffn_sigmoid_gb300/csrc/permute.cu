@@ -14,6 +14,8 @@
 #include <cuda_fp16.h>
 
 #include "moe_kernels.h"
+#include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -24,6 +26,7 @@ __global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restri
                                                          int E, int k,
                                                          int32_t* __restrict__ blockcnt) {
   __shared__ int cnt[kMaxE];
+  pdl_wait();
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * kPermTokBlock;
@@ -36,26 +39,7 @@ __global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restri
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
-}
-
-// Exclusive scan of n values in shared memory by warp 0 (n <= a few hundred).
-__device__ void warp0_exclusive_scan(int* v, int n, int* total) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  int carry = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const int x = i < n ? v[i] : 0;
-    int incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (i < n) v[i] = carry + incl - x;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) *total = carry;
+  pdl_launch_dependents();
 }
 
 // One CTA of 1024 threads.
@@ -68,6 +52,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
   __shared__ int ntile[kMaxE + 1];
   __shared__ int n_entries;
   __shared__ int total_rows;
+  pdl_wait();
   const int nblk = (T + kPermTokBlock - 1) / kPermTokBlock;
   // per expert: running sum over blocks (becomes the block-relative base)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -110,6 +95,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
     }
   }
   if (threadIdx.x == 0) table[0] = n_entries;
+  pdl_launch_dependents();
 }
 
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __restrict__ idx,
@@ -120,6 +106,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ row_of,
                                                            float* __restrict__ roww) {
   __shared__ uint32_t bits[kMaxE][kWordsPerBlock];
+  pdl_wait();
   for (int i = threadIdx.x; i < E * kWordsPerBlock; i += blockDim.x) (&bits[0][0])[i] = 0u;
   __syncthreads();
   const int t0 = blockIdx.x * kPermTokBlock;
@@ -150,15 +137,26 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
     gather[r] = t0 + tl;
     if (roww) roww[r] = 1.0f;
   }
+  pdl_launch_dependents();
 }
 
 // One warp per row, grid-stride.  H is a multiple of 128, so a row is a whole
-// number of 16-byte chunks.
+// number of 16-byte chunks.  When zero_out is set, the kernel also clears the
+// layer output (zero_n floats) that the down kernel later adds into.
 template <bool kToFp16>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ gather,
                                                           int rows, int H, int T,
-                                                          uint16_t* __restrict__ x_perm) {
+                                                          uint16_t* __restrict__ x_perm,
+                                                          float4* __restrict__ zero_out,
+                                                          size_t zero_n4) {
+  pdl_wait();
+  if (zero_out) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_n4;
+         i += stride)
+      zero_out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int chunks = H / 8;
@@ -183,6 +181,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
       dst[c] = v;
     }
   }
+  pdl_launch_dependents();
 }
 
 // Tile table from an offsets array (E+2 entries), one CTA.  Offsets are
@@ -196,6 +195,7 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
   __shared__ int lo[kMaxE + 1];
   __shared__ int ntile[kMaxE + 1];
   __shared__ int n_entries;
+  pdl_wait();
   for (int g = threadIdx.x; g <= E; g += blockDim.x) {
     const int a = min(max(offsets[g], 0), rows);
     const int b = min(max(offsets[g + 1], a), rows);
@@ -220,6 +220,83 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
     }
   }
   if (threadIdx.x == 0) table[0] = min(n_entries, capacity);
+  pdl_launch_dependents();
+}
+
+// Decode-size routing in one CTA (T <= kSmallT tokens): per-token top-k,
+// expert histogram, exclusive offsets (shared expert appended as group E),
+// stable ranks from per-expert token bitmaps, gather / row_of / row weights
+// and the tile table -- the work of the top-k, count, scan and scatter
+// kernels without three launches in between.
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
+    const float* __restrict__ z, int T, int E, int k, int BN, int32_t* __restrict__ idx_out,
+    float* __restrict__ w_out, int32_t* __restrict__ offsets, int32_t* __restrict__ gather,
+    int32_t* __restrict__ row_of, float* __restrict__ roww, int32_t* __restrict__ table) {
+  __shared__ int s_idx[kSmallT * kMaxTopK];
+  __shared__ float s_w[kSmallT * kMaxTopK];
+  __shared__ int cnt[kMaxE + 2];
+  __shared__ int ntile[kMaxE + 1];
+  __shared__ uint32_t bits[kMaxE][kSmallT / 32];
+  __shared__ int total_rows, n_entries;
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) cnt[g] = 0;
+  for (int i = threadIdx.x; i < E * (kSmallT / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < T; t += kSmallThreads / 32) {
+    int e;
+    float wv;
+    warp_topk(z + static_cast<size_t>(t) * E, E, k, &e, &wv);
+    if (lane < k) {
+      s_idx[t * k + lane] = e;
+      s_w[t * k + lane] = wv;
+      idx_out[t * k + lane] = e;
+      w_out[t * k + lane] = wv;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k, e = s_idx[i];
+    atomicAdd(&cnt[e], 1);
+    atomicOr(&bits[e][t >> 5], 1u << (t & 31));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) cnt[E] = T;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (cnt[g] + BN - 1) / BN;
+  warp0_exclusive_scan(cnt, E + 1, &total_rows);  // cnt becomes the offsets
+  __syncthreads();
+  if (threadIdx.x == 0) cnt[E + 1] = total_rows;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E + 1; g += blockDim.x) offsets[g] = cnt[g];
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k, e = s_idx[i];
+    int rank = __popc(bits[e][t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bits[e][wd]);
+    const int r = cnt[e] + rank;
+    gather[r] = t;
+    row_of[i] = r;
+    roww[r] = s_w[i];
+  }
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    gather[k * T + t] = t;
+    roww[k * T + t] = 1.0f;
+  }
+  warp0_exclusive_scan(ntile, E + 1, &n_entries);
+  __syncthreads();
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int o = cnt[g], c = cnt[g + 1] - o;
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      TileEntry te;
+      te.group = g;
+      te.row0 = o + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = n_entries;
+  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -227,41 +304,50 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
 cudaError_t launch_perm_count(const int32_t* idx, int T, int E, int k, int32_t* blockcnt,
                               cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  perm_count_kernel<<<(T + kPermTokBlock - 1) / kPermTokBlock, 256, 0, s>>>(idx, T, E, k,
-                                                                            blockcnt);
-  return cudaGetLastError();
+  return launch_pdl(perm_count_kernel, dim3((T + kPermTokBlock - 1) / kPermTokBlock), dim3(256),
+                    0, s, idx, T, E, k, blockcnt);
 }
 
 cudaError_t launch_perm_scan(int32_t* blockcnt, int T, int E, int k, int32_t* offsets,
                              int32_t* table, int BN, cudaStream_t s) {
-  perm_scan_kernel<<<1, 1024, 0, s>>>(blockcnt, T, E, k, offsets, table, BN);
-  return cudaGetLastError();
+  return launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, blockcnt, T, E, k, offsets, table,
+                    BN);
 }
 
 cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_t* blockbase,
                                 int T, int E, int k, int32_t* gather, int32_t* row_of,
                                 float* roww, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  perm_scatter_kernel<<<(T + kPermTokBlock - 1) / kPermTokBlock, 256, 0, s>>>(
-      idx, w, blockbase, T, E, k, gather, row_of, roww);
-  return cudaGetLastError();
+  return launch_pdl(perm_scatter_kernel, dim3((T + kPermTokBlock - 1) / kPermTokBlock), dim3(256),
+                    0, s, idx, w, blockbase, T, E, k, gather, row_of, roww);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
-                               bool to_fp16, uint16_t* x_perm, cudaStream_t s) {
+                               bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
+                               cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int blocks = min((rows + 7) / 8, 152 * 8);
+  float4* z4 = reinterpret_cast<float4*>(zero_out);
+  const size_t n4 = zero_n / 4;
   if (to_fp16)
-    gather_rows_kernel<true><<<blocks, 256, 0, s>>>(x, gather, rows, H, T, x_perm);
-  else
-    gather_rows_kernel<false><<<blocks, 256, 0, s>>>(x, gather, rows, H, T, x_perm);
-  return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel<true>, dim3(blocks), dim3(256), 0, s, x, gather, rows, H,
+                      T, x_perm, z4, n4);
+  return launch_pdl(gather_rows_kernel<false>, dim3(blocks), dim3(256), 0, s, x, gather, rows, H,
+                    T, x_perm, z4, n4);
 }
 
 cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,
                                       int32_t* table, int BN, cudaStream_t s) {
-  table_from_offsets_kernel<<<1, 1024, 0, s>>>(offsets, E, rows, capacity, table, BN);
-  return cudaGetLastError();
+  return launch_pdl(table_from_offsets_kernel, dim3(1), dim3(1024), 0, s, offsets, E, rows,
+                    capacity, table, BN);
+}
+
+cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
+                               float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
+                               float* roww, int32_t* table, cudaStream_t s) {
+  if (T == 0 || T > kSmallT) return cudaErrorInvalidValue;
+  return launch_pdl(route_small_kernel, dim3(1), dim3(kSmallThreads), 0, s, z, T, E, k, BN, idx,
+                    w, offsets, gather, row_of, roww, table);
 }
 
 }  // namespace moe

@@ -1,0 +1,114 @@
+// Device building blocks shared by the router and permutation kernels: the
+// warp top-k of one token's logits and a warp-0 exclusive scan.
+#pragma once
+
+#include <stdint.h>
+
+#include "moe_kernels.h"
+
+namespace moe {
+
+// Order-preserving map of a float onto uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+constexpr int kTopkVPL = kMaxE / 32;  // logits held per lane
+
+// Top-k of one token's E logits by one warp ("Top-8 expert selection",
+// sigmoid routing and "Weight normalization": "Add GLM-5.3-Flash (glm5next)
+// support with ROCmFP mix qtypes (105/106)", section "MoE FFN (REAL routed
+// expert execution)"; ties to the lower index: deterministic top-k, "feat(glm53):
+// add device-resident HIP backend for MI350P", "Key changes").
+// Lane L holds experts L, L+32, ...; each round takes the warp maximum of the
+// 64-bit key (score key << 32 | ~e): the larger score wins and an exact tie
+// goes to the lower expert index.  Lane j < k ends with slot j: *e_out, and
+// *w_out = sigmoid(z_j) / sum of the k sigmoids.
+__device__ __forceinline__ void warp_topk(const float* __restrict__ zr, int E, int k, int* e_out,
+                                          float* w_out) {
+  const int lane = threadIdx.x & 31;
+  uint32_t keys[kTopkVPL];
+#pragma unroll
+  for (int i = 0; i < kTopkVPL; ++i) {
+    const int e = i * 32 + lane;
+    keys[i] = e < E ? float_key(zr[e]) : 0u;
+  }
+  uint32_t taken = 0;
+  int my_e = 0;
+  float my_z = 0.f;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < kTopkVPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < E && !((taken >> i) & 1u)) {
+        const uint64_t key =
+            (static_cast<uint64_t>(keys[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+        best = key > best ? key : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    const int e_win = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+    if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
+    if (lane == j) {
+      my_e = e_win;
+      my_z = key_float(static_cast<uint32_t>(best >> 32));
+    }
+  }
+  const float s = lane < k ? 1.0f / (1.0f + expf(-my_z)) : 0.f;
+  float sum = s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  *e_out = my_e;
+  *w_out = s / sum;
+}
+
+// Exclusive scan of n values in shared memory by warp 0; *total gets the sum.
+// Other threads return at once; the caller synchronises.
+__device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const int x = i < n ? v[i] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (i < n) v[i] = carry + incl - x;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) *total = carry;
+}
+
+// Launch helper: programmatic stream serialization lets a kernel begin while
+// its predecessor drains; every kernel launched this way calls pdl_wait()
+// before it touches data a predecessor produced.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace moe

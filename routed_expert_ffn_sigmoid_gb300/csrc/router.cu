@@ -10,12 +10,15 @@
 #include <cuda_bf16.h>
 
 #include "moe_kernels.h"
+#include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouterWarps = 8;    // experts per CTA (one per warp)
+constexpr int kRouterWarps = 4;    // experts per CTA (one per warp)
 constexpr int kRouterTokTile = 8;  // tokens per CTA
+constexpr int kLoadBatch = 8;      // 16-byte router loads in flight per lane
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -26,15 +29,17 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-// grid (ceil(E / 8), ceil(T / 8)), 256 threads.  The CTA stages its 8 token
-// rows in shared memory; each warp streams one router row with 16-byte loads
-// and keeps 8 fp32 partial sums, reduced across the warp at the end.
-__global__ void __launch_bounds__(256) router_logits_simt_kernel(const uint16_t* __restrict__ x,
+// grid (ceil(E / 4), ceil(T / 8)), 128 threads.  The CTA stages its 8 token
+// rows in shared memory; each warp streams one router row, issuing 8 16-byte
+// loads per lane before using any of them, and keeps 8 fp32 partial sums,
+// reduced across the warp at the end.
+__global__ void __launch_bounds__(128) router_logits_simt_kernel(const uint16_t* __restrict__ x,
                                                                  const uint16_t* __restrict__ wr,
                                                                  const float* __restrict__ b,
                                                                  float* __restrict__ z, int T,
                                                                  int H, int E) {
   extern __shared__ uint4 xs[];  // [kRouterTokTile][H / 8]
+  pdl_wait();
   const int chunks = H / 8;
   const int t0 = blockIdx.y * kRouterTokTile;
   const int nt = min(kRouterTokTile, T - t0);
@@ -44,96 +49,65 @@ __global__ void __launch_bounds__(256) router_logits_simt_kernel(const uint16_t*
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterWarps + warp;
-  if (e >= E) return;
-  float acc[kRouterTokTile];
+  if (e < E) {
+    float acc[kRouterTokTile];
 #pragma unroll
-  for (int t = 0; t < kRouterTokTile; ++t) acc[t] = 0.f;
-  const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e) * H);
-  for (int c = lane; c < chunks; c += 32) {
-    float wf[8];
-    bf16x8_to_f32(__ldg(wrow + c), wf);
+    for (int t = 0; t < kRouterTokTile; ++t) acc[t] = 0.f;
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e) * H);
+    for (int c0 = lane; c0 < chunks; c0 += 32 * kLoadBatch) {
+      uint4 wv[kLoadBatch];
 #pragma unroll
-    for (int t = 0; t < kRouterTokTile; ++t) {
-      if (t < nt) {
-        float xf[8];
-        bf16x8_to_f32(xs[t * chunks + c], xf);
+      for (int i = 0; i < kLoadBatch; ++i) {
+        const int c = c0 + 32 * i;
+        wv[i] = c < chunks ? __ldg(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[t] = fmaf(xf[i], wf[i], acc[t]);
+      for (int i = 0; i < kLoadBatch; ++i) {
+        const int c = c0 + 32 * i;
+        if (c < chunks) {
+          float wf[8];
+          bf16x8_to_f32(wv[i], wf);
+#pragma unroll
+          for (int t = 0; t < kRouterTokTile; ++t) {
+            if (t < nt) {
+              float xf[8];
+              bf16x8_to_f32(xs[t * chunks + c], xf);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[t] = fmaf(xf[j], wf[j], acc[t]);
+            }
+          }
+        }
       }
     }
-  }
-  const float bias = b[e];
+    const float bias = b[e];
 #pragma unroll
-  for (int t = 0; t < kRouterTokTile; ++t) {
-    float v = acc[t];
+    for (int t = 0; t < kRouterTokTile; ++t) {
+      float v = acc[t];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0 && t < nt) z[static_cast<size_t>(t0 + t) * E + e] = v + bias;
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t < nt) z[static_cast<size_t>(t0 + t) * E + e] = v + bias;
+    }
   }
+  pdl_launch_dependents();
 }
 
-// Order-preserving map of a float onto uint32 (larger float -> larger key).
-__device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-constexpr int kVPL = kMaxE / 32;  // values per lane
-
-// One warp per token.  Lane L holds experts L, L+32, ...; each of the k rounds
-// takes the warp-wide maximum of the 64-bit key (score key << 32 | ~e), so the
-// larger score wins and an exact tie goes to the lower expert index.  Slot j
-// ends in lane j, which applies the sigmoid; the warp sums the k scores and
-// each slot is divided by the sum.
+// One warp per token: top-k, sigmoid, renormalisation.
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ z, int T, int E,
                                                    int k, int32_t* __restrict__ idx,
                                                    float* __restrict__ w) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* zr = z + static_cast<size_t>(t) * E;
-  uint32_t keys[kVPL];
-#pragma unroll
-  for (int i = 0; i < kVPL; ++i) {
-    const int e = i * 32 + lane;
-    keys[i] = e < E ? float_key(__ldg(zr + e)) : 0u;
-  }
-  uint32_t taken = 0;
-  int my_e = 0;
-  float my_z = 0.f;
-  for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int i = 0; i < kVPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u)) {
-        const uint64_t key = (static_cast<uint64_t>(keys[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
-        best = key > best ? key : best;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e_win = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
-    if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
-    if (lane == j) {
-      my_e = e_win;
-      my_z = key_float(static_cast<uint32_t>(best >> 32));
+  if (t < T) {
+    int e;
+    float wv;
+    warp_topk(z + static_cast<size_t>(t) * E, E, k, &e, &wv);
+    if (lane < k) {
+      idx[static_cast<size_t>(t) * k + lane] = e;
+      w[static_cast<size_t>(t) * k + lane] = wv;
     }
   }
-  const float s = lane < k ? 1.0f / (1.0f + expf(-my_z)) : 0.f;
-  float sum = s;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    idx[static_cast<size_t>(t) * k + lane] = my_e;
-    w[static_cast<size_t>(t) * k + lane] = s / sum;
-  }
+  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -146,16 +120,15 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_route
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  dim3 grid((E + kRouterWarps - 1) / kRouterWarps, (T + kRouterTokTile - 1) / kRouterTokTile);
-  router_logits_simt_kernel<<<grid, 256, smem, s>>>(x, w_router, b, z, T, H, E);
-  return cudaGetLastError();
+  const dim3 grid((E + kRouterWarps - 1) / kRouterWarps, (T + kRouterTokTile - 1) / kRouterTokTile);
+  return launch_pdl(router_logits_simt_kernel, grid, dim3(32 * kRouterWarps), smem, s, x,
+                    w_router, b, z, T, H, E);
 }
 
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(z, T, E, k, idx, w);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, z, T, E, k, idx, w);
 }
 
 }  // namespace moe

@@ -89,9 +89,10 @@ def test_argument_errors_before_any_launch(L):
     bad = moe.make_dims(8, 200, 288, 64)
     assert _call_forward(bad, need) == moe.MOE_ERR_UNSUPPORTED
     assert L.moe_ffn_forward(None, 0, 0, 0, None, None, 0, 0, 0, None) == moe.MOE_ERR_INVALID_ARG
-    # Int4 weights need their scale pointers
-    d4 = moe.make_dims(8, 256, 288, 64, fmt="int4")
+    # Int4 weights need their scale pointers, and H, I multiples of 256
+    d4 = moe.make_dims(8, 256, 288, 256, fmt="int4")
     assert _call_forward(d4, moe.moe_workspace_size(d4)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_workspace_size(moe.make_dims(8, 256, 288, 64, fmt="int4")) == 0
 
 
 def test_zero_tokens_is_a_no_op(L):
