@@ -142,8 +142,8 @@ bool encode_kmajor(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uin
 // Weight stacks are always addressed as 3-D maps (a 2-D map ignores the third
 // coordinate, so the shared expert's leading dimension of 1 is fine).
 bool encode_weights(CUtensorMap* m, const void* base, bool bf16, uint64_t K, uint64_t N,
-                    uint64_t n_experts) {
-  const uint32_t box_rows = N < 128 ? static_cast<uint32_t>(N) : 128u;
+                    uint64_t n_experts, uint32_t max_box_rows = 128) {
+  const uint32_t box_rows = N < max_box_rows ? static_cast<uint32_t>(N) : max_box_rows;
   const EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {K, N, n_experts};
@@ -349,6 +349,61 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     D.budget_ns = kWaitBudgetNs;
     D.grid = max_entries * D.mblocks < nsm ? max_entries * D.mblocks : nsm;
     const cudaError_t e = launch_int4_gemm(D, s);
+    record(ev, 4, s);
+    return from_cuda(e);
+  }
+
+  if (BN == 128 && d.I % 128 == 0 && d.H % 256 == 0) {
+    // token-major kernels: tiles of up to 128 rows of one group
+    TmLaunch G{};
+    if (!encode_kmajor(&G.tm_a[0], x_perm, true, d.H, rows, 1, 128) ||
+        !encode_weights(&G.tm_b[0], ex->gate, true, d.H, d.I, d.E, 128) ||
+        !encode_weights(&G.tm_b[1], ex->up, true, d.H, d.I, d.E, 128) ||
+        !encode_weights(&G.tm_sb[0], sh->gate, true, d.H, d.I, 1, 128) ||
+        !encode_weights(&G.tm_sb[1], sh->up, true, d.H, d.I, 1, 128))
+      return MOE_ERR_CUDA;
+    G.tm_a[1] = G.tm_a[0];
+    G.table = table;
+    G.gateup = true;
+    G.K = d.H;
+    G.N_out = d.I;
+    G.nblocks = d.I / 128;
+    G.E = d.E;
+    G.total_rows = rows;
+    G.out_rows = d.T;
+    G.epilogue = kEpiStoreRows;
+    G.h0 = ws.at<void>(ws.L.h0);
+    G.h1 = ws.at<void>(ws.L.h1);
+    G.status = ws.status();
+    G.budget_ns = kWaitBudgetNs;
+    G.grid = max_entries * G.nblocks < nsm ? max_entries * G.nblocks : nsm;
+    record(ev, 2, s);
+    if (launch_tm_gemm(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(ev, 3, s);
+    TmLaunch D{};
+    if (!encode_kmajor(&D.tm_a[0], G.h0, true, d.I, rows, 1, 128) ||
+        !encode_kmajor(&D.tm_a[1], G.h1, true, d.I, rows, 1, 128) ||
+        !encode_weights(&D.tm_b[0], ex->down, true, d.I, d.H, d.E, 256) ||
+        !encode_weights(&D.tm_sb[0], sh->down, true, d.I, d.H, 1, 256))
+      return MOE_ERR_CUDA;
+    D.tm_b[1] = D.tm_b[0];
+    D.tm_sb[1] = D.tm_sb[0];
+    D.table = table;
+    D.gateup = false;
+    D.K = d.I;
+    D.N_out = d.H;
+    D.nblocks = d.H / 256;
+    D.E = d.E;
+    D.total_rows = rows;
+    D.out_rows = d.T;
+    D.epilogue = epilogue;
+    D.gather = gather;
+    D.roww = roww;
+    D.out = out;
+    D.status = ws.status();
+    D.budget_ns = kWaitBudgetNs;
+    D.grid = max_entries * D.nblocks < nsm ? max_entries * D.nblocks : nsm;
+    const cudaError_t e = launch_tm_gemm(D, s);
     record(ev, 4, s);
     return from_cuda(e);
   }

@@ -1,0 +1,313 @@
+// Token-major grouped expert GEMMs for large token counts (bf16 weights).
+//
+// Same per-expert computation as expert_gemm.cu (gate/up with the clamped
+// SwiGLU; down with the routing weight and the scatter-add into the output;
+// "Add GLM-5.3-Flash (glm5next) support with ROCmFP mix qtypes (105/106)",
+// section "MoE FFN (REAL routed expert execution)"), oriented for groups of
+// ~100+ tokens: the 128 token rows of a tile entry are the MMA's M operand
+// and weight features are N (2 x 128 for gate/up, 256 for down).  Every MMA
+// is full width, shared-memory operand bytes per flop drop by ~1.5x for the
+// down projection, and the epilogue owns one token row per thread, so h is
+// written with 16-byte stores and the output with 16-byte vector atomics.
+//
+// CTA = 6 warps (TMA producer, MMA issuer, 4 epilogue warps), persistent over
+// (tile-table entry, feature block) pairs, accumulators double-buffered in
+// TMEM, every wait bounded as in the other GEMM kernels.
+#include <cuda_bf16.h>
+
+#include "moe_kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;            // token rows per tile
+constexpr int kBK = 64;
+constexpr int kRowBytes = kBK * 2;  // 128
+constexpr int kATileBytes = kBM * kRowBytes;  // 16 KB per token plane
+constexpr int kStageBudget = 224 * 1024;
+constexpr int kThreads = 192;
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// NA token planes (gate/up: x; down: h hi + lo), NBM weight matrices of
+// FN features each (gate/up: 2 x 128; down: 1 x 256).
+template <int NA, int NBM, int FN>
+struct TmCfg {
+  static constexpr int kBTileBytes = FN * kRowBytes;
+  static constexpr int kStageBytes = NA * kATileBytes + NBM * kBTileBytes;
+  static constexpr int kStages = cmin(6, kStageBudget / kStageBytes);
+  static constexpr int kAccCols = NBM * FN;  // 256 in both uses
+  static constexpr int kAccStages = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static_assert(kAccStages * kAccCols <= 512, "TMEM");
+  static_assert(kStageBytes % 1024 == 0, "alignment");
+};
+
+struct TmArgs {
+  const int32_t* table;
+  int K, N_out, nblocks, E, total_rows, out_rows;
+  const int32_t* gather;
+  const float* roww;
+  float* out;
+  void* h0;
+  void* h1;
+  int* status;
+  uint64_t budget_ns;
+};
+
+__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int i) {
+  const int4 v =
+      reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + kTableHeaderBytes)[i];
+  return TileEntry{v.x, v.y, v.z, v.w};
+}
+
+__device__ __forceinline__ float clamped_swiglu(float g, float u) {
+  const float gc = fminf(g, 10.0f);
+  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
+  return gc / (1.0f + expf(-gc)) * uc;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// EPI: kEpiStoreRows with NBM == 2 means the gate/up SwiGLU epilogue writing
+// h (hi/lo bf16 planes); with NBM == 1, kEpiScatterAdd / kEpiStoreRows are the
+// down epilogues.
+template <int NA, int NBM, int FN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                   const __grid_constant__ CUtensorMap tm_a1,
+                   const __grid_constant__ CUtensorMap tm_b0,
+                   const __grid_constant__ CUtensorMap tm_b1,
+                   const __grid_constant__ CUtensorMap tm_sb0,
+                   const __grid_constant__ CUtensorMap tm_sb1, const TmArgs a) {
+  using Cfg = TmCfg<NA, NBM, FN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + Cfg::kStages * Cfg::kStageBytes);
+  uint64_t* empty = full + Cfg::kStages;
+  uint64_t* tfull = empty + Cfg::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const AbortState ab{abort_flag, a.status, a.budget_ns};
+
+  pdl_wait();
+  pdl_launch_dependents();
+  const int total = a.table[0] * a.nblocks;
+  const int KB = a.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, tile / a.nblocks);
+        const int nb = tile % a.nblocks;
+        const bool sh = te.group == a.E;
+        const int ge = sh ? 0 : te.group;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(st, &tm_a0, &full[stage], kb * kBK, te.row0, pol_x);
+          if (NA == 2) tma_load_2d(st + kATileBytes, &tm_a1, &full[stage], kb * kBK, te.row0, pol_x);
+          uint8_t* sb = st + NA * kATileBytes;
+          tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &full[stage], kb * kBK, nb * FN, ge, pol_w);
+          if (NBM == 2)
+            tma_load_3d(sb + Cfg::kBTileBytes, sh ? &tm_sb1 : &tm_b1, &full[stage], kb * kBK,
+                        nb * FN, ge, pol_w);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < Cfg::kStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kBM, FN, true);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ab)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + acc * Cfg::kAccCols;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = smem_u32(tiles + stage * Cfg::kStageBytes);
+          const uint64_t da0 = sw128_kmajor_desc(st);
+          const uint64_t da1 = sw128_kmajor_desc(st + kATileBytes);
+          const uint64_t db0 = sw128_kmajor_desc(st + NA * kATileBytes);
+          const uint64_t db1 = sw128_kmajor_desc(st + NA * kATileBytes + Cfg::kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t accum = (kb | k) != 0;
+            umma_f16(d0, da0 + 2 * k, db0 + 2 * k, idesc, accum);
+            if (NA == 2) umma_f16(d0, da1 + 2 * k, db0 + 2 * k, idesc, 1u);
+            if (NBM == 2) umma_f16(d0 + FN, da0 + 2 * k, db1 + 2 * k, idesc, accum);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;  // token row of the tile this thread owns
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileEntry te = entry_at(a.table, tile / a.nblocks);
+      const int nb = tile % a.nblocks;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
+      tc_fence_after_sync();
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
+      const int r = te.row0 + lrow;
+      const bool valid = lrow < te.nrows && r < a.total_rows;
+      int t = 0;
+      float wr = 0.f;
+      if (EPI == kEpiScatterAdd && valid) {
+        t = a.gather[r];
+        wr = a.roww[r];
+      }
+      const bool live = valid && (EPI != kEpiScatterAdd || (t >= 0 && t < a.out_rows));
+      for (int c0 = 0; c0 < FN; c0 += 16) {
+        uint32_t v0[16], v1[16];
+        tmem_ld_32x32b_x16(tq + c0, v0);
+        if (NBM == 2) tmem_ld_32x32b_x16(tq + FN + c0, v1);
+        tmem_ld_wait();
+        if (!live) continue;
+        const int f = nb * FN + c0;  // first feature of this chunk
+        if (NBM == 2) {
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float h0 = clamped_swiglu(__uint_as_float(v0[2 * i]), __uint_as_float(v1[2 * i]));
+            const float h1 =
+                clamped_swiglu(__uint_as_float(v0[2 * i + 1]), __uint_as_float(v1[2 * i + 1]));
+            const __nv_bfloat16 a0 = __float2bfloat16_rn(h0), a1 = __float2bfloat16_rn(h1);
+            hi[i] = pack_bf16x2(a0, a1);
+            lo[i] = pack_bf16x2(__float2bfloat16_rn(h0 - __bfloat162float(a0)),
+                                __float2bfloat16_rn(h1 - __bfloat162float(a1)));
+          }
+          uint4* ph = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.h0) +
+                                               static_cast<size_t>(r) * a.N_out + f);
+          uint4* pl = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.h1) +
+                                               static_cast<size_t>(r) * a.N_out + f);
+          ph[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          ph[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          pl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          pl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        } else if (EPI == kEpiScatterAdd) {
+          float4* po = reinterpret_cast<float4*>(a.out + static_cast<size_t>(t) * a.N_out + f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            atomicAdd(po + i, make_float4(wr * __uint_as_float(v0[4 * i]),
+                                          wr * __uint_as_float(v0[4 * i + 1]),
+                                          wr * __uint_as_float(v0[4 * i + 2]),
+                                          wr * __uint_as_float(v0[4 * i + 3])));
+        } else {
+          float4* po = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * a.N_out + f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            po[i] = make_float4(__uint_as_float(v0[4 * i]), __uint_as_float(v0[4 * i + 1]),
+                                __uint_as_float(v0[4 * i + 2]), __uint_as_float(v0[4 * i + 3]));
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <int NA, int NBM, int FN, int EPI>
+cudaError_t tm_dispatch(const TmLaunch& L, cudaStream_t s) {
+  using Cfg = TmCfg<NA, NBM, FN>;
+  auto kern = tm_gemm_kernel<NA, NBM, FN, EPI>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  TmArgs a{L.table, L.K, L.N_out, L.nblocks, L.E, L.total_rows, L.out_rows,
+           L.gather, L.roww, L.out, L.h0, L.h1, L.status, L.budget_ns};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_a[0], L.tm_a[1], L.tm_b[0], L.tm_b[1], L.tm_sb[0],
+                            L.tm_sb[1], a);
+}
+
+}  // namespace
+
+cudaError_t launch_tm_gemm(const TmLaunch& L, cudaStream_t s) {
+  if (L.gateup) return tm_dispatch<1, 2, 128, kEpiStoreRows>(L, s);
+  if (L.epilogue == kEpiScatterAdd) return tm_dispatch<2, 1, 256, kEpiScatterAdd>(L, s);
+  return tm_dispatch<2, 1, 256, kEpiStoreRows>(L, s);
+}
+
+}  // namespace moe

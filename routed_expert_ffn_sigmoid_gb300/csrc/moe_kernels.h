@@ -131,6 +131,26 @@ struct Int4Launch {
 };
 cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
 
+// Token-major grouped GEMM (bf16, token tiles of 128 rows): gate/up with the
+// SwiGLU epilogue (h hi/lo planes) or down with the scatter-add / store-rows
+// epilogue.  tm_a: token planes (x_perm; or h hi, h lo), tm_b / tm_sb: weight
+// stacks of the routed / shared experts (gate, up; or down).
+struct TmLaunch {
+  CUtensorMap tm_a[2], tm_b[2], tm_sb[2];
+  const int32_t* table;
+  bool gateup;
+  int K, N_out, nblocks, E, total_rows, out_rows, epilogue;
+  const int32_t* gather;
+  const float* roww;
+  float* out;
+  void* h0;
+  void* h1;
+  int* status;
+  uint64_t budget_ns;
+  int grid;
+};
+cudaError_t launch_tm_gemm(const TmLaunch& L, cudaStream_t s);
+
 // Diagnostic bounded wait on a barrier nothing completes.
 cudaError_t launch_wait_selftest(int* status, uint64_t budget_ns, cudaStream_t s);
 

@@ -147,9 +147,9 @@ def test_expert_ffn_tiny(tiny):
     assert rel_max_err(y, ref) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("T", [8, 64])
+@pytest.mark.parametrize("T", [8, 64, 200])
 def test_expert_ffn_decode(decode, T):
-    x = decode.inp.x[:T]
+    x = decode.inp.x[:T] if T <= decode.wl.T else _gapped(decode, T)
     y, off, gather, _, _ = _run_expert_ffn(decode, x)
     inp = decode.inp
     rows = int(off[-1])
