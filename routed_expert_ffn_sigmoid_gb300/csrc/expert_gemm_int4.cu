@@ -22,7 +22,9 @@
 //                    layout the MMA reads
 //   warp 14, lane 0  activation producer: TMA of the token rows (fp16)
 // The raw ring is as deep as shared memory allows (its stages are what carry
-// the HBM bytes); two to four operand slots decouple dequantisation from MMA.
+// the HBM bytes); two to four fp16 weight slots decouple dequantisation from
+// the MMA; the activation tiles have a ring of their own, refilled as soon as
+// the MMA has read them, so their loads run as far ahead as the code loads.
 // Operand slots carry two barriers, one for the activation bytes (TMA) and
 // one for the 128 dequantiser arrivals, so that after an abort every copy
 // still in flight can be waited for on its own barrier.
@@ -60,15 +62,20 @@ constexpr int ceil_pow2_32(int v) {
 
 template <int BN, int NA>
 struct Int4Cfg {
-  static constexpr int kSlotBytes = NA * kATileBytes + BN * kRowBytes;
+  static constexpr int kSlotBytes = NA * kATileBytes;
+  static constexpr int kBTileBytes = BN * kRowBytes;
+  static constexpr int kBStages = BN <= 16 ? 8 : (BN <= 64 ? 6 : 4);
+  static constexpr int kBRingBytes = kBStages * kBTileBytes;
   static constexpr int kRawBytes = NA * (kCodeTileBytes + kScaleTileBytes);
-  static constexpr int kRaw = cmin(NA == 2 ? 4 : 6, (kBudget - 2 * kSlotBytes) / kRawBytes);
-  static constexpr int kSlots = cmin(4, (kBudget - kRaw * kRawBytes) / kSlotBytes);
+  static constexpr int kRaw =
+      cmin(NA == 2 ? 4 : 6, (kBudget - kBRingBytes - 2 * kSlotBytes) / kRawBytes);
+  static constexpr int kSlots = cmin(4, (kBudget - kBRingBytes - kRaw * kRawBytes) / kSlotBytes);
   static constexpr int kAccStages = (2 * NA * BN <= 512) ? 2 : 1;
   static constexpr int kAccCols = NA * BN;
   static constexpr int kTmemCols = ceil_pow2_32(kAccStages * kAccCols);
-  static constexpr int kSmemBytes = kSlots * kSlotBytes + kRaw * kRawBytes + 1024 + 512;
-  static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte alignment");
+  static constexpr int kSmemBytes = kSlots * kSlotBytes + kBRingBytes + kRaw * kRawBytes + 1024 + 512;
+  static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0 && kBTileBytes % 1024 == 0,
+                "1024-byte alignment");
   static_assert(kSlots >= 2 && kRaw >= 2, "at least two operand slots and raw stages");
 };
 
@@ -138,12 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* slots = base;
-  uint8_t* raws = base + Cfg::kSlots * Cfg::kSlotBytes;
+  uint8_t* bring = base + Cfg::kSlots * Cfg::kSlotBytes;
+  uint8_t* raws = bring + Cfg::kBRingBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raws + Cfg::kRaw * Cfg::kRawBytes);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + Cfg::kRaw;
   uint64_t* b_full = raw_empty + Cfg::kRaw;
-  uint64_t* a_full = b_full + Cfg::kSlots;
+  uint64_t* b_empty = b_full + Cfg::kBStages;
+  uint64_t* a_full = b_empty + Cfg::kBStages;
   uint64_t* op_empty = a_full + Cfg::kSlots;
   uint64_t* tfull = op_empty + Cfg::kSlots;
   uint64_t* tempty = tfull + 2;
@@ -157,8 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kDqThreads);
     }
-    for (int i = 0; i < Cfg::kSlots; ++i) {
+    for (int i = 0; i < Cfg::kBStages; ++i) {
       mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < Cfg::kSlots; ++i) {
       mbar_init(&a_full[i], kDqThreads);
       mbar_init(&op_empty[i], 1);
     }
@@ -191,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return raws + rs * Cfg::kRawBytes + NA * kCodeTileBytes + m * kScaleTileBytes;
   };
   auto a_tile = [&](int os, int m) { return slots + os * Cfg::kSlotBytes + m * kATileBytes; };
-  auto b_tile = [&](int os) { return slots + os * Cfg::kSlotBytes + NA * kATileBytes; };
+  auto b_tile = [&](int bs) { return bring + bs * Cfg::kBTileBytes; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- raw producer
@@ -236,30 +248,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- activation producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      int os = 0;
-      uint32_t oph = 0, armed = 0, armed_par = 0;
+      int bs = 0;
+      uint32_t bph = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileEntry te = entry_at(a.table, tile / a.mblocks);
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
+          if (!mbar_wait(&b_empty[bs], bph ^ 1u, ab)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&b_full[os], nchunks * kChunkBytes);
-          armed |= 1u << os;
-          armed_par = (armed_par & ~(1u << os)) | (oph << os);
+          mbar_arrive_expect_tx(&b_full[bs], nchunks * kChunkBytes);
+          armed |= 1u << bs;
+          armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
           for (int c = 0; c < nchunks; ++c)
-            tma_load_2d(b_tile(os) + c * kChunkBytes, &tm_b, &b_full[os], kb * kBK,
+            tma_load_2d(b_tile(bs) + c * kChunkBytes, &tm_b, &b_full[bs], kb * kBK,
                         te.row0 + c * kChunkRows, pol);
-          if (++os == Cfg::kSlots) {
-            os = 0;
-            oph ^= 1u;
+          if (++bs == Cfg::kBStages) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
       }
-      for (int s = 0; s < Cfg::kSlots; ++s)
+      for (int s = 0; s < Cfg::kBStages; ++s)
         if ((armed >> s) & 1u) mbar_wait_drain(&b_full[s], (armed_par >> s) & 1u);
     }
   } else if (warp >= 6 && warp < kDqWarpEnd) {
@@ -321,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc0 = idesc_f16(kBM, 16, false) & ~(0x3Fu << 17);
-      int os = 0, acc = 0;
-      uint32_t oph = 0, acc_phase = 0;
+      int os = 0, bs = 0, acc = 0;
+      uint32_t oph = 0, bph = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileEntry te = entry_at(a.table, tile / a.mblocks);
@@ -331,12 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + acc * Cfg::kAccCols;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&b_full[os], oph, ab) || !mbar_wait(&a_full[os], oph, ab)) {
+          if (!mbar_wait(&b_full[bs], bph, ab) || !mbar_wait(&a_full[os], oph, ab)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(os)));
+          const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(bs)));
           const uint64_t da0 = sw128_kmajor_desc(smem_u32(a_tile(os, 0)));
           const uint64_t da1 = sw128_kmajor_desc(smem_u32(a_tile(os, NA - 1)));
 #pragma unroll
@@ -346,9 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (NA == 2) umma_f16(d0 + BN, da1 + 2 * k, db + 2 * k, idesc, accum);
           }
           umma_commit(&op_empty[os]);
+          umma_commit(&b_empty[bs]);
           if (++os == Cfg::kSlots) {
             os = 0;
             oph ^= 1u;
+          }
+          if (++bs == Cfg::kBStages) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
         if (!ok) break;
