@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 1
+#define MOE_FFN_ABI_VERSION 2
 
 /* A cudaStream_t, spelled without the CUDA headers. */
 typedef struct CUstream_st* moe_stream_t;
@@ -74,9 +74,14 @@ typedef enum moe_wfmt {
   MOE_W_INT4_G32 = 1         /* offset-binary Int4, bf16 scale per 32 elements */
 } moe_wfmt;
 
+/* Behaviour flags (moe_dims.flags). */
+#define MOE_FLAG_DETERMINISTIC 1  /* fixed-order combination: bitwise reproducible output */
+#define MOE_FLAG_ACCUMULATE 2     /* out += layer(x) (out holds e.g. the residual on entry) */
+
 typedef struct moe_dims {
   int32_t T, H, E, I, I_shared, top_k;
   int32_t fmt;               /* moe_wfmt */
+  int32_t flags;             /* MOE_FLAG_* bits; 0 = defaults */
 } moe_dims;
 
 typedef struct moe_weights {
@@ -148,7 +153,8 @@ moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* 
  * Weighted combination in a fixed order ("Weighted combination of expert
  * outputs", lucebox PR #1, "What Executes vs. TODO" item 3):
  *   out[t] = sum_{j=0..top_k-1} topk_w[t][j] * y_perm[row_of[t][j]] + y_perm[top_k*T + t]
- * out fp32 [T][H] is overwritten.  Bitwise reproducible run to run.
+ * out fp32 [T][H] is overwritten, or, with MOE_FLAG_ACCUMULATE, added to
+ * (its entry value first, then the slots in order).  Bitwise reproducible.
  */
 moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* row_of,
                        const float* topk_w, float* out, moe_stream_t stream);
@@ -156,9 +162,18 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
 /*
  * The whole layer, fused: router/top-k, permutation, grouped gate/up with the
  * clamped SwiGLU epilogue, grouped down whose epilogue multiplies by the
- * routing weight and adds into out (fp32 [T][H], overwritten), with the
- * shared expert run as one more group of weight 1.  The fp32 additions into
- * out are atomic, so the last bits may differ run to run.
+ * routing weight and adds into out (fp32 [T][H]), with the shared expert run
+ * as one more group of weight 1.  By default out is overwritten and the fp32
+ * additions into it are atomic, so the last bits may differ run to run.
+ * Flags (moe_dims.flags):
+ *   MOE_FLAG_DETERMINISTIC  the down GEMM stores unweighted rows into the
+ *       workspace and a fixed-order combination (slot 0..top_k-1, then the
+ *       shared expert) writes out: bitwise identical run to run; the
+ *       workspace grows by (top_k+1)*T*H*4 bytes.
+ *   MOE_FLAG_ACCUMULATE  out += layer(x): out's contents on entry (e.g. the
+ *       residual stream, "Residual connections" around the FFN in "Add
+ *       GLM-5.3-Flash (glm5next) support with ROCmFP mix qtypes (105/106)",
+ *       "What Executes vs. TODO") are added to, not replaced.
  */
 moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_router,
                            const float* b_router, const moe_weights* experts,
@@ -188,6 +203,21 @@ moe_status moe_ffn_forward_timed(const moe_dims* d, const void* x, const void* w
                                  const moe_weights* shared, float* out, void* ws,
                                  size_t ws_bytes, const moe_stage_events* events,
                                  moe_stream_t stream);
+
+/*
+ * Dense FFN (the first dense layers of the model, "Dense FFN for layers 0-2
+ * (no experts)", lucebox PR #1, "MoE FFN" section) through the same grouped
+ * tensor-core GEMMs, all T tokens as one group:
+ *   out[t] = Wd . (silu(min(Wg x_t, 10)) * clamp(Wu x_t, -10, 10))
+ * d->T, H, I (the dense intermediate size), fmt and flags are used; E, I_shared
+ * and top_k are ignored.  weights: gate, up [1][I][H], down [1][H][I] in the
+ * format d->fmt (Int4: with scales).  out fp32 [T][H] is overwritten, or
+ * added to with MOE_FLAG_ACCUMULATE; each element gets one contribution, so
+ * the result is reproducible run to run.  ws: moe_dense_workspace_size(d).
+ */
+size_t moe_dense_workspace_size(const moe_dims* d);
+moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* weights, float* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Synchronises `stream`, returns the device status word that kernels using

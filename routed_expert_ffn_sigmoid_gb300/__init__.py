@@ -29,11 +29,14 @@ MOE_W_BF16 = 0
 MOE_W_INT4_G32 = 1
 FMT = {"bf16": MOE_W_BF16, "int4": MOE_W_INT4_G32}
 
+MOE_FLAG_DETERMINISTIC = 1
+MOE_FLAG_ACCUMULATE = 2
+
 # every symbol include/moe_ffn.h declares
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_size", "moe_router_topk",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
            "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout",
-           "moe_router_topk_static_scratch")
+           "moe_router_topk_static_scratch", "moe_dense_workspace_size", "moe_dense_ffn")
 
 # T * E limit of moe_router_topk_static_scratch (floats of its fixed scratch)
 MOE_STATIC_ROUTER_LOGITS = 1 << 18
@@ -45,7 +48,7 @@ STAGE_NAMES = ("router_topk", "permute", "gateup_swiglu", "down_scatter")
 class MoeDims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32), ("top_k", ctypes.c_int32),
-                ("fmt", ctypes.c_int32)]
+                ("fmt", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -94,6 +97,8 @@ def lib() -> ctypes.CDLL:
                 "moe_workspace_status": ([vp, vp], i32),
                 "moe_debug_wait_timeout": ([vp, u64, vp], i32),
                 "moe_router_topk_static_scratch": ([pd, vp, vp, vp, vp, vp, vp], i32),
+                "moe_dense_workspace_size": ([pd], sz),
+                "moe_dense_ffn": ([pd, vp, pw, vp, vp, sz, vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -128,9 +133,9 @@ def _stream(stream):
 
 
 def make_dims(T: int, H: int, E: int, I: int, I_shared: int | None = None, top_k: int = 8,
-              fmt: str | int = "bf16") -> MoeDims:
+              fmt: str | int = "bf16", flags: int = 0) -> MoeDims:
     fmt = FMT[fmt] if isinstance(fmt, str) else int(fmt)
-    return MoeDims(T, H, E, I, I if I_shared is None else I_shared, top_k, fmt)
+    return MoeDims(T, H, E, I, I if I_shared is None else I_shared, top_k, fmt, flags)
 
 
 def make_weights(gate, up, down, gate_scale=None, up_scale=None, down_scale=None) -> MoeWeights:
@@ -205,3 +210,14 @@ def moe_router_topk_static_scratch(dims, x, w_router, b_router, topk_idx, topk_w
                                                 _ptr(b_router), _ptr(topk_idx), _ptr(topk_w),
                                                 _stream(stream)),
            "moe_router_topk_static_scratch")
+
+
+def moe_dense_workspace_size(dims: MoeDims) -> int:
+    return int(lib().moe_dense_workspace_size(ctypes.byref(dims)))
+
+
+def moe_dense_ffn(dims, x, weights: MoeWeights, out, ws, stream=None):
+    """Dense FFN (clamped SwiGLU) of all T tokens through the grouped GEMMs."""
+    _check(lib().moe_dense_ffn(ctypes.byref(dims), _ptr(x), ctypes.byref(weights), _ptr(out),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_dense_ffn")

@@ -21,7 +21,7 @@ constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, total;
+  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, y_perm, total;
 };
 
 int rows_of(const moe_dims& d) { return (d.top_k + 1) * d.T; }
@@ -62,6 +62,7 @@ Layout layout_of(const moe_dims& d) {
   L.x_perm = take(rows * H * 2);
   L.h0 = take(rows * I * 2);
   L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
+  L.y_perm = take((d.flags & MOE_FLAG_DETERMINISTIC) ? rows * H * 4 : 0);
   L.total = o;
   return L;
 }
@@ -73,6 +74,7 @@ moe_status check_dims(const moe_dims* d) {
   if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->I <= 0 || d->I_shared <= 0 || d->top_k <= 0)
     return MOE_ERR_INVALID_ARG;
   if (d->fmt != MOE_W_BF16 && d->fmt != MOE_W_INT4_G32) return MOE_ERR_UNSUPPORTED;
+  if (d->flags & ~(MOE_FLAG_DETERMINISTIC | MOE_FLAG_ACCUMULATE)) return MOE_ERR_INVALID_ARG;
   if (d->H % 128 != 0 || d->H > 12288) return MOE_ERR_UNSUPPORTED;
   if (d->I % 64 != 0 || d->I_shared != d->I) return MOE_ERR_UNSUPPORTED;
   if (d->E > kMaxE || d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED;
@@ -492,6 +494,10 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   float* roww = w.at<float>(L.roww);
   int32_t* table = w.at<int32_t>(L.table);
   void* x_perm = w.at<void>(L.x_perm);
+  const bool det = (d->flags & MOE_FLAG_DETERMINISTIC) != 0;
+  const bool accumulate = (d->flags & MOE_FLAG_ACCUMULATE) != 0;
+  // out is cleared by the gather kernel only when the down epilogue adds into it
+  float* zero_out = (det || accumulate) ? nullptr : out;
   record(ev, 0, s);
   if (d->T <= kSmallT) {
     // decode sizes: logits, then one CTA for top-k + the whole permutation
@@ -502,18 +508,49 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
                            table, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T,
-                           d->fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), out,
-                           static_cast<size_t>(d->T) * d->H, s) != cudaSuccess)
+                           d->fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
+                           zero_out ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
     if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
     record(ev, 1, s);
     if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather,
-                          w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, out)) != MOE_OK)
+                          w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, zero_out)) != MOE_OK)
       return st;
   }
-  return run_experts(*d, x_perm, table, experts, shared, kEpiScatterAdd, gather, roww, out, w, s,
-                     ev);
+  if (!det)
+    return run_experts(*d, x_perm, table, experts, shared, kEpiScatterAdd, gather, roww, out, w, s,
+                       ev);
+  // deterministic: unweighted rows, then the fixed-order combination
+  float* y_perm = w.at<float>(L.y_perm);
+  if ((st = run_experts(*d, x_perm, table, experts, shared, kEpiStoreRows, nullptr, nullptr, y_perm,
+                        w, s, ev)) != MOE_OK)
+    return st;
+  const cudaError_t e = launch_combine(y_perm, w.at<int32_t>(L.row_of), wts, d->T, d->H,
+                                       d->top_k, accumulate, out, s);
+  record(ev, 4, s);
+  return from_cuda(e);
+}
+
+// Dims of the dense FFN as a one-group problem: group 0 = all T rows.
+moe_dims dense_dims(const moe_dims& d) {
+  moe_dims dd = d;
+  dd.E = 1;
+  dd.top_k = 0;
+  dd.I_shared = d.I;
+  dd.flags = 0;
+  return dd;
+}
+
+moe_status check_dense_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->I <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->fmt != MOE_W_BF16 && d->fmt != MOE_W_INT4_G32) return MOE_ERR_UNSUPPORTED;
+  if (d->flags & ~(MOE_FLAG_DETERMINISTIC | MOE_FLAG_ACCUMULATE)) return MOE_ERR_INVALID_ARG;
+  if (d->H % 128 != 0 || d->H > 12288 || d->I % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d->fmt == MOE_W_INT4_G32 && (d->H % 256 != 0 || d->I % 256 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (d->T > (1 << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -602,7 +639,8 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
   if (!y_perm || !row_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK) return st;
-  return from_cuda(launch_combine(y_perm, row_of, topk_w, d->T, d->H, d->top_k, out,
+  return from_cuda(launch_combine(y_perm, row_of, topk_w, d->T, d->H, d->top_k,
+                                  (d->flags & MOE_FLAG_ACCUMULATE) != 0, out,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -621,6 +659,43 @@ moe_status moe_ffn_forward_timed(const moe_dims* d, const void* x, const void* w
                                  moe_stream_t stream) {
   return forward_impl(d, x, w_router, b_router, experts, shared, out, ws, ws_bytes, events,
                       stream);
+}
+
+size_t moe_dense_workspace_size(const moe_dims* d) {
+  if (check_dense_dims(d) != MOE_OK) return 0;
+  return layout_of(dense_dims(*d)).total;
+}
+
+moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* weights, float* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_dense_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(weights, d->fmt)) return MOE_ERR_INVALID_ARG;
+  const moe_dims dd = dense_dims(*d);
+  Ws w;
+  if ((st = check_ws(dd, ws, ws_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* gather = w.at<int32_t>(w.L.gather);
+  float* roww = w.at<float>(w.L.roww);
+  int32_t* table = w.at<int32_t>(w.L.table);
+  if (launch_dense_rows(d->T, pick_bn(d->T), gather, roww, table, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!(d->flags & MOE_FLAG_ACCUMULATE) &&
+      cudaMemsetAsync(out, 0, static_cast<size_t>(d->T) * d->H * sizeof(float), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const void* rows = x;
+  if (d->fmt == MOE_W_INT4_G32) {  // the Int4 GEMMs take fp16 activations
+    if (launch_gather_rows(static_cast<const uint16_t*>(x), gather, d->T, d->H, d->T, true,
+                           w.at<uint16_t>(w.L.x_perm), nullptr, 0, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    rows = w.at<void>(w.L.x_perm);
+  }
+  // one contribution per output element: the atomic add onto zero (or onto
+  // the caller's values) gives the same bits on every run
+  return run_experts(dd, rows, table, weights, weights, kEpiScatterAdd, gather, roww, out, w, s);
 }
 
 moe_status moe_workspace_status(void* ws, moe_stream_t stream) {

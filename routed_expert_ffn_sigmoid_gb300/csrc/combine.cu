@@ -4,7 +4,10 @@
 // GLM-5.3-Flash (glm5next) support with ROCmFP mix qtypes (105/106)",
 // section "What Executes vs. TODO", item 3).  Every output element is summed
 // by one thread in slot order, so the result is the same bits on every run.
+// With `accumulate`, the sum starts from out's entry value (a residual).
 #include "moe_kernels.h"
+#include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -12,9 +15,11 @@ namespace {
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ w, int T, int H,
-                                                      int k, float* __restrict__ out) {
+                                                      int k, bool accumulate,
+                                                      float* __restrict__ out) {
   __shared__ int rows[kMaxTopK + 1];
   __shared__ float wt[kMaxTopK];
+  pdl_wait();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
     if (threadIdx.x < k) {
@@ -25,7 +30,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     __syncthreads();
     const int n4 = H / 4;
     for (int c = threadIdx.x; c < n4; c += blockDim.x) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = accumulate ? reinterpret_cast<const float4*>(out + static_cast<size_t>(t) * H)[c]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < k; ++j) {
         const float4 v = reinterpret_cast<const float4*>(y + static_cast<size_t>(rows[j]) * H)[c];
         acc.x = fmaf(wt[j], v.x, acc.x);
@@ -46,11 +52,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }  // namespace
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* row_of, const float* w, int T,
-                           int H, int k, float* out, cudaStream_t s) {
+                           int H, int k, bool accumulate, float* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int blocks = T < 152 * 8 ? T : 152 * 8;
-  combine_kernel<<<blocks, 256, 0, s>>>(y_perm, row_of, w, T, H, k, out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, y_perm, row_of, w, T, H, k,
+                    accumulate, out);
 }
 
 }  // namespace moe

@@ -55,6 +55,10 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int row
 cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
                                float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
                                float* roww, int32_t* table, cudaStream_t s);
+// Dense FFN: rows 0..T-1 are one group (group 0): gather[r] = r, roww[r] = 1
+// and a tile table of ceil(T / BN) entries.
+cudaError_t launch_dense_rows(int T, int BN, int32_t* gather, float* roww, int32_t* table,
+                              cudaStream_t s);
 // Tile table from existing offsets (for the unfused expert entry point);
 // at most `capacity` entries.
 cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,
@@ -63,7 +67,7 @@ cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, i
 // ---------------------------------------------------------------- combine
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* row_of, const float* w, int T,
-                           int H, int k, float* out, cudaStream_t s);
+                           int H, int k, bool accumulate, float* out, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMMs
 

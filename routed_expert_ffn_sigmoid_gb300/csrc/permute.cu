@@ -350,4 +350,39 @@ cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int3
                     w, offsets, gather, row_of, roww, table);
 }
 
+namespace {
+
+__global__ void __launch_bounds__(256) dense_rows_kernel(int T, int BN, int32_t* __restrict__ gather,
+                                                         float* __restrict__ roww,
+                                                         int32_t* __restrict__ table) {
+  pdl_wait();
+  const int n = (T + BN - 1) / BN;
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T || i < n; i += gridDim.x * blockDim.x) {
+    if (i < T) {
+      gather[i] = i;
+      roww[i] = 1.0f;
+    }
+    if (i < n) {
+      TileEntry te;
+      te.group = 0;
+      te.row0 = i * BN;
+      te.nrows = min(BN, T - i * BN);
+      te.pad = 0;
+      ent[i] = te;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) table[0] = n;
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_dense_rows(int T, int BN, int32_t* gather, float* roww, int32_t* table,
+                              cudaStream_t s) {
+  const int blocks = min((T + 255) / 256, 152 * 4);
+  return launch_pdl(dense_rows_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, T, BN,
+                    gather, roww, table);
+}
+
 }  // namespace moe

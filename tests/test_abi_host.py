@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     for code in range(6):
         assert moe.moe_status_string(code).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)
@@ -53,8 +53,15 @@ def test_workspace_size(L):
     for bad in (moe.make_dims(8, 200, 288, 64), moe.make_dims(8, 256, 288, 96),
                 moe.make_dims(8, 256, 600, 64), moe.make_dims(8, 256, 288, 64, top_k=17),
                 moe.make_dims(-1, 256, 288, 64), moe.make_dims(8, 256, 288, 64, I_shared=128),
-                moe.make_dims(8, 256, 4, 64, top_k=8), moe.make_dims(8, 256, 288, 64, fmt=7)):
+                moe.make_dims(8, 256, 4, 64, top_k=8), moe.make_dims(8, 256, 288, 64, fmt=7),
+                moe.make_dims(8, 256, 288, 64, flags=4)):
         assert moe.moe_workspace_size(bad) == 0
+    # the deterministic mode keeps (top_k+1)*T*H fp32 rows in the workspace
+    det = moe.make_dims(64, 4096, 288, 1536, flags=moe.MOE_FLAG_DETERMINISTIC)
+    assert moe.moe_workspace_size(det) - big >= rows * 4096 * 4
+    dense = moe.make_dims(64, 4096, 0, 10240)
+    assert moe.moe_dense_workspace_size(dense) >= 64 * 10240 * 4
+    assert moe.moe_dense_workspace_size(moe.make_dims(64, 4000, 0, 10240)) == 0
 
 
 class _Fake:
