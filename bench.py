@@ -191,6 +191,12 @@ def parse():
     ap.add_argument("--tokens", type=int, default=64)
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small profiling cases only)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="fixed-order combination (bitwise reproducible output)")
+    ap.add_argument("--accumulate", action="store_true",
+                    help="out += layer(x) (residual add into the output)")
+    ap.add_argument("--dense-ffn", type=int, default=0, metavar="I",
+                    help="time the dense FFN (intermediate size I) instead of the MoE layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
@@ -203,9 +209,15 @@ def dist_env():
     return rank, world, local
 
 
-def config_of(wl, world):
+def config_of(wl, world, args=None):
+    modes = []
+    if args is not None and args.deterministic:
+        modes.append("deterministic combination")
+    if args is not None and args.accumulate:
+        modes.append("residual accumulate")
     return {"workload": f"{wl.name} T={wl.T} H={wl.H} E={wl.E} top_k={wl.top_k} I={wl.I} "
                         f"shared I={wl.I_shared} {wl.fmt} weights",
+            "modes": modes or ["default (atomic fp32 scatter-add)"],
             "tokens_per_step": wl.T, "weights": wl.fmt,
             "expert_weight_bytes": wl.E * expert_bytes(wl),
             "x_batches_cycled": N_BATCHES,
@@ -251,6 +263,7 @@ def run_reference(args, wl, rank, world):
 def run_ours(args, wl, rank, world, local):
     import torch
     import routed_expert_ffn_sigmoid_gb300 as moe
+    from routed_expert_ffn_sigmoid_gb300 import replicas
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -273,9 +286,11 @@ def run_ours(args, wl, rank, world, local):
                            ex.get("up_scale"), ex.get("down_scale"))
     shw = moe.make_weights(sh["gate"], sh["up"], sh["down"], sh.get("gate_scale"),
                            sh.get("up_scale"), sh.get("down_scale"))
-    dims = moe.make_dims(wl.T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
+    flags = ((moe.MOE_FLAG_DETERMINISTIC if args.deterministic else 0)
+             | (moe.MOE_FLAG_ACCUMULATE if args.accumulate else 0))
+    dims = moe.make_dims(wl.T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, flags)
     ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
-    out = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+    out = torch.zeros((wl.T, wl.H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -325,14 +340,7 @@ def run_ours(args, wl, rank, world, local):
 
     step_ms = [evs[0].elapsed_time(evs[nst]) for evs, _ in step_events]
     stage_ms = [[evs[i].elapsed_time(evs[i + 1]) for evs, _ in step_events] for i in range(nst)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    tokens_total = wl.T * args.steps * world
-    value = tokens_total / (total_ms / 1e3)
+    value, ms_per_step = replicas.job_throughput(sum(step_ms), wl.T, args.steps, world, dev)
 
     # end to end through the C ABI with host buffers: H2D x, layer, D2H out
     host_x = [torch.from_numpy(bt.view(np.int16)).pin_memory() for bt in batches]
@@ -354,7 +362,7 @@ def run_ours(args, wl, rank, world, local):
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    e2e_value = wl.T * args.steps * world / (e2e_ms / 1e3)
+    e2e_value, _ = replicas.job_throughput(e2e_ms, wl.T, args.steps, world, dev)
 
     hbm_peak, tc_peak, tc_sust, peak_src = peaks()
     mean_distinct = sum(distinct[s % N_BATCHES] for s in range(args.steps)) / args.steps
@@ -382,7 +390,7 @@ def run_ours(args, wl, rank, world, local):
             "dtype": "bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
                      "int4 weights dequantised to fp16, fp32 accumulate",
             "data": "synthetic (seeded generator; random-init weights)",
-            "config": config_of(wl, world),
+            "config": config_of(wl, world, args),
             "roofline": {"bound": "hbm", "kernel": "gateup_swiglu (tcgen05 grouped gate/up)",
                          "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
@@ -397,12 +405,100 @@ def run_ours(args, wl, rank, world, local):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
-            "gpu_launches": 8 * args.steps,
+            # T <= 128: logits, one-CTA routing, gather, gate/up, down; larger T:
+            # logits, top-k, count, scan, scatter, gather, gate/up, down;
+            # + the fixed-order combination in the deterministic mode
+            "gpu_launches": ((5 if wl.T <= 128 else 8) + (1 if args.deterministic else 0))
+                            * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_dense(args, rank, world, local):
+    """Times moe_dense_ffn: the dense FFN of the first layers (H = 4096,
+    intermediate size --dense-ffn) over T tokens, weights resident."""
+    import torch
+    import routed_expert_ffn_sigmoid_gb300 as moe
+    from routed_expert_ffn_sigmoid_gb300 import replicas
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    base = synthetic.WORKLOADS[args.workload]
+    I = args.dense_ffn
+    wl = synthetic.Workload("dense_ffn", args.tokens, base.H, 1, I, I, base.top_k, base.fmt, 60,
+                            tokens=(args.tokens,))
+    w = synthetic.gen_experts(wl, shared=True)
+    x_all = synthetic.gen_x(wl, T=wl.T * N_BATCHES)
+
+    def up(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t if a.dtype == np.uint8 else t.view(torch.int16)).to(dev)
+
+    dw = {k: up(v) for k, v in w.items()}
+    weights = moe.make_weights(dw["gate"], dw["up"], dw["down"], dw.get("gate_scale"),
+                               dw.get("up_scale"), dw.get("down_scale"))
+    xs = [up(x_all[i * wl.T:(i + 1) * wl.T]) for i in range(N_BATCHES)]
+    flags = moe.MOE_FLAG_ACCUMULATE if args.accumulate else 0
+    dims = moe.make_dims(wl.T, wl.H, 0, I, I, wl.top_k, wl.fmt, flags)
+    ws = torch.zeros(moe.moe_dense_workspace_size(dims), dtype=torch.uint8, device=dev)
+    out = torch.zeros((wl.T, wl.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for s_ in range(args.warmup):
+        moe.moe_dense_ffn(dims, xs[s_ % N_BATCHES], weights, out, ws)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        for s_ in range(args.steps):
+            flush.zero_()
+            evs[s_][0].record(stream)
+            moe.moe_dense_ffn(dims, xs[s_ % N_BATCHES], weights, out, ws)
+            evs[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+    st = moe.moe_workspace_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.moe_status_string(st))
+    total = sum(a.elapsed_time(b) for a, b in evs)
+    value, ms_per_step = replicas.job_throughput(total, wl.T, args.steps, world, dev)
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+    wbytes = 3 * wl.H * I * (2 if wl.fmt == "bf16" else 0.5 + 2 / 32)
+    nbytes = wbytes + wl.T * wl.H * (2 + 4)
+    flops = 2 * 3 * wl.H * I * wl.T
+    gbs = nbytes / (ms_per_step / 1e3) / 1e9
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    ridge = tc_sust * 1e12 / (hbm_peak * 1e9)
+    bound = "hbm" if flops / nbytes < ridge else "tensor"
+    if rank == 0:
+        roof = ({"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                 "frac": gbs / hbm_peak} if bound == "hbm" else
+                {"bound": "tensor", "achieved": tflops, "peak": tc_sust, "unit": "TFLOP/s",
+                 "frac": tflops / tc_sust})
+        roof.update({"kernel": "moe_dense_ffn (grouped gate/up + down, one group)",
+                     "traffic": None, "peak_source": f"{peak_src} peaks",
+                     "algorithmic_bytes_per_call": nbytes, "flops_per_call": flops})
+        print(json.dumps({
+            "metric": "dense FFN tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
+                     "int4 weights dequantised to fp16, fp32 accumulate",
+            "data": "synthetic (seeded generator; random-init weights)",
+            "config": {"workload": f"dense FFN T={wl.T} H={wl.H} I={I} {wl.fmt} weights",
+                       "l2": "flushed before every step (512 MB write)"},
+            "roofline": roof, "gbs": gbs, "tflops": tflops,
+            # dense-rows table, gate/up, down (+ the fp16 conversion of x for Int4)
+            "gpu_launches": (3 + (1 if wl.fmt != "bf16" else 0)) * args.steps,
+            "clocks": clk.summary()}), flush=True)
 
 
 def main():
@@ -414,6 +510,8 @@ def main():
         wl = replace(wl, E=args.experts)
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
+    elif args.dense_ffn:
+        run_dense(args, rank, world, local)
     else:
         run_ours(args, wl, rank, world, local)
 
