@@ -212,8 +212,11 @@ moe_status moe_ffn_forward_timed(const moe_dims* d, const void* x, const void* w
  * d->T, H, I (the dense intermediate size), fmt and flags are used; E, I_shared
  * and top_k are ignored.  weights: gate, up [1][I][H], down [1][H][I] in the
  * format d->fmt (Int4: with scales).  out fp32 [T][H] is overwritten, or
- * added to with MOE_FLAG_ACCUMULATE; each element gets one contribution, so
- * the result is reproducible run to run.  ws: moe_dense_workspace_size(d).
+ * added to with MOE_FLAG_ACCUMULATE.  When few tiles would leave SMs idle the
+ * down projection is split along K and its parts added atomically, so the
+ * last bits may vary run to run; with MOE_FLAG_DETERMINISTIC it is not split
+ * and every output element gets one contribution (bitwise reproducible).
+ * ws: moe_dense_workspace_size(d).
  */
 size_t moe_dense_workspace_size(const moe_dims* d);
 moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* weights, float* out,

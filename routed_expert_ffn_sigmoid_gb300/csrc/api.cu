@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/moe_ffn.h"
@@ -21,7 +22,10 @@ constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, y_perm, total;
+  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, y_perm;
+  size_t partial, counters;
+  size_t partial_units;  // K-split units the partial buffer holds (0: no split possible)
+  size_t total;
 };
 
 int rows_of(const moe_dims& d) { return (d.top_k + 1) * d.T; }
@@ -38,6 +42,33 @@ size_t table_bytes(const moe_dims& d) {
   // bounded by (E + 1) + rows / 16
   const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 15) / 16;
   return kTableHeaderBytes + entries * sizeof(TileEntry);
+}
+
+constexpr int kMaxSplit = 8;
+constexpr int kSplitTileLimit = 1024;  // tile counts from which no split is considered
+
+// Upper bound on the gate/up tiles of the weight-rows-as-M kernels: at most
+// one entry per row and per (group, BN rows).
+int gateup_tiles_bound(const moe_dims& d) {
+  const int rows = rows_of(d);
+  const int BN = pick_bn(d.T);
+  // the dense FFN (top_k == 0) is exactly one group of rows
+  const int entries = d.top_k == 0 ? (rows + BN - 1) / BN
+                                   : std::min((d.E + 1) + (rows + BN - 1) / BN, rows);
+  return entries * ((d.I + 127) / 128);
+}
+
+// Units per tile along K: enough units for every SM and a last wave at
+// least half full; 1 when the tiles alone fill several waves.
+int split_for(long tiles, int KB, int nsm) {
+  if (tiles <= 0 || tiles >= 4L * nsm) return 1;
+  for (int S = 1; S <= kMaxSplit && KB / S >= 4; ++S) {
+    const long units = tiles * S;
+    if (units < nsm) continue;
+    const long full = units / nsm, rem = units % nsm;
+    if (rem == 0 || 2 * rem >= nsm || full >= 4) return S;
+  }
+  return 1;
 }
 
 Layout layout_of(const moe_dims& d) {
@@ -63,6 +94,10 @@ Layout layout_of(const moe_dims& d) {
   L.h0 = take(rows * I * 2);
   L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
   L.y_perm = take((d.flags & MOE_FLAG_DETERMINISTIC) ? rows * H * 4 : 0);
+  const int tiles = gateup_tiles_bound(d);
+  L.partial_units = tiles < kSplitTileLimit ? static_cast<size_t>(tiles) * kMaxSplit : 0;
+  L.partial = take(L.partial_units * 2 * pick_bn(d.T) * 128 * 4);
+  L.counters = take(L.partial_units ? static_cast<size_t>(tiles) * 4 : 0);
   L.total = o;
   return L;
 }
@@ -243,6 +278,7 @@ moe_status run_logits(const moe_dims& d, const void* x, const void* w_router, co
     L.out_rows = d.T;
     L.bf16 = true;
     L.epilogue = kEpiRouter;
+    L.ksplit = 1;
     L.bias = b;
     L.out = z;
     L.status = ws.status();
@@ -431,8 +467,14 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
   G.status = ws.status();
   G.budget_ns = kWaitBudgetNs;
   {
-    const int tiles = max_entries * ((d.I + 127) / 128);
-    G.grid = tiles < nsm ? tiles : nsm;
+    const int tiles = gateup_tiles_bound(d);
+    int S = split_for(tiles, d.H / 64, nsm);
+    if (static_cast<size_t>(tiles) * S > ws.L.partial_units) S = 1;
+    G.ksplit = S;
+    G.partial = ws.at<float>(ws.L.partial);
+    G.counters = ws.at<int>(ws.L.counters);
+    const long units = static_cast<long>(tiles) * S;
+    G.grid = units < nsm ? static_cast<int>(units) : nsm;
   }
   record(ev, 2, s);
   cudaError_t e = launch_gateup(G, s);
@@ -465,8 +507,14 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
   D.status = ws.status();
   D.budget_ns = kWaitBudgetNs;
   {
-    const int tiles = max_entries * D.mblocks;
-    D.grid = tiles < nsm ? tiles : nsm;
+    const int entries = d.top_k == 0 ? (rows + BN - 1) / BN : std::min(max_entries, rows);
+    const long tiles = static_cast<long>(entries) * D.mblocks;
+    // a split down projection adds its parts atomically (order varies), so
+    // not in the deterministic mode
+    D.ksplit = (epilogue == kEpiScatterAdd && !(d.flags & MOE_FLAG_DETERMINISTIC))
+                   ? split_for(tiles, d.I / 64, nsm) : 1;
+    const long units = tiles * D.ksplit;
+    D.grid = units < nsm ? static_cast<int>(units) : nsm;
   }
   e = launch_down(D, s);
   record(ev, 4, s);
@@ -538,7 +586,7 @@ moe_dims dense_dims(const moe_dims& d) {
   dd.E = 1;
   dd.top_k = 0;
   dd.I_shared = d.I;
-  dd.flags = 0;
+  dd.flags = d.flags & MOE_FLAG_DETERMINISTIC;
   return dd;
 }
 

@@ -72,6 +72,9 @@ struct DownCfg {
 struct GateUpArgs {
   const int32_t* table;
   int K, I, E, a_rows, total_rows;
+  int ksplit;            // units per tile along K (1: no split)
+  float* partial;        // ksplit > 1: fp32 partial G/U per unit
+  int* counters;         // ksplit > 1: finished units per tile (zero between calls)
   void* h0;
   void* h1;
   int* status;
@@ -81,6 +84,7 @@ struct GateUpArgs {
 struct DownArgs {
   const int32_t* table;
   int dense_rows;
+  int ksplit;            // units per tile along K (scatter-add epilogue only)
   int K, N_out, mblocks, E, a_rows, total_rows, out_rows;
   const int32_t* gather;
   const float* roww;
@@ -105,6 +109,11 @@ __device__ __forceinline__ TileEntry entry_at(const int32_t* table, int dense_ro
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
+constexpr int kEpiThread0 = 64;  // first epilogue thread (warp 2)
+
+// Barrier among the four epilogue warps only.
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // silu(min(g, 10)) * clamp(u, -10, 10)
 __device__ __forceinline__ float clamped_swiglu(float g, float u) {
   const float gc = fminf(g, 10.0f);
@@ -117,6 +126,7 @@ struct SmemCarve {
   uint64_t *full, *empty, *tfull, *tempty, *drain;
   uint32_t* tmem_holder;
   int* abort_flag;
+  int* split_flags;  // [0]: an epilogue warp gave up, [1]: this unit finishes its tile
 };
 
 __device__ __forceinline__ SmemCarve carve(uint8_t* raw, int stages, int stage_bytes) {
@@ -129,6 +139,7 @@ __device__ __forceinline__ SmemCarve carve(uint8_t* raw, int stages, int stage_b
   c.drain = c.tempty + 2;
   c.tmem_holder = reinterpret_cast<uint32_t*>(c.drain + 1);
   c.abort_flag = reinterpret_cast<int*>(c.tmem_holder + 1);
+  c.split_flags = c.abort_flag + 1;
   return c;
 }
 
@@ -143,6 +154,8 @@ __device__ __forceinline__ void init_barriers(const SmemCarve& c, int stages) {
   }
   mbar_init(c.drain, 1);
   *c.abort_flag = 0;
+  c.split_flags[0] = 0;
+  c.split_flags[1] = 0;
   fence_barrier_init();
 }
 
@@ -187,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   const int mblocks = (a.I + kBM - 1) / kBM;
   const int total = n_entries_of(a.table, 0, BN) * mblocks;
+  const int units = total * a.ksplit;
   const int KB = a.K / kBK;
 
   if (warp == 0) {
@@ -195,7 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int tile = u / a.ksplit, sp = u % a.ksplit;
+        const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
         const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
         const int mb = tile % mblocks;
         const bool sh = te.group == a.E;
@@ -204,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ge = sh ? 0 : te.group;
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
         const uint32_t bytes = 2u * a.a_rows * kRowBytes + nchunks * kChunkBytes;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab)) {
             ok = false;
             break;
@@ -234,14 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int tile = u / a.ksplit, sp = u % a.ksplit;
+        const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
         const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
         const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
         if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, ab)) break;
         tc_fence_after_sync();
         const uint32_t d_g = tmem_base + acc * Cfg::kAccCols;
         const uint32_t d_u = d_g + BN;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, ab)) {
             ok = false;
             break;
@@ -253,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = sw128_kmajor_desc(st + 2 * kATileBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t accum = (kb | k) != 0;
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
             umma_f16(d_g, dg + 2 * k, db + 2 * k, idesc, accum);
             umma_f16(d_u, du + 2 * k, db + 2 * k, idesc, accum);
           }
@@ -280,9 +298,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int tile = u / a.ksplit;
       const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
       const int mb = tile % mblocks;
+      if (a.ksplit > 1) {
+        // Split along K: this unit's partial G and U go to global memory; the
+        // last unit of the tile to finish adds the partials up in split order
+        // (so the sum is the same whichever unit is last) and applies the
+        // SwiGLU.  Nothing waits on another CTA: the counter only decides who
+        // finishes.  Every epilogue warp reaches every epilogue_bar(), also
+        // after a failed wait, so a timeout cannot strand one at a barrier.
+        const bool ok_w = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[acc], acc_phase, ab));
+        if (!ok_w && lane == 0) sm.split_flags[0] = 1;
+        epilogue_bar();
+        if (sm.split_flags[0]) break;
+        tc_fence_after_sync();
+        const int fl = q * 32 + lane;
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
+        const int n = round16(te.nrows);
+        float* pu = a.partial + static_cast<size_t>(u) * 2 * BN * kBM;
+        for (int c0 = 0; c0 < n; c0 += 16) {
+          uint32_t g[16], uv[16];
+          tmem_ld_32x32b_x16(tq + c0, g);
+          tmem_ld_32x32b_x16(tq + BN + c0, uv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pu[static_cast<size_t>(c0 + i) * kBM + fl] = __uint_as_float(g[i]);
+            pu[static_cast<size_t>(BN + c0 + i) * kBM + fl] = __uint_as_float(uv[i]);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&sm.tempty[acc]);
+        __threadfence();
+        epilogue_bar();
+        if (threadIdx.x == kEpiThread0)
+          sm.split_flags[1] = atomicAdd(&a.counters[tile], 1) == a.ksplit - 1;
+        epilogue_bar();
+        if (sm.split_flags[1]) {
+          __threadfence();
+          const int f = mb * kBM + fl;
+          const float* pt = a.partial + static_cast<size_t>(tile) * a.ksplit * 2 * BN * kBM;
+          if (f < a.I) {
+            // 16 token columns at a time: 32 independent loads per split step
+            for (int c0 = 0; c0 < te.nrows; c0 += 16) {
+              float gs[16], us[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) gs[i] = us[i] = 0.f;
+              for (int p2 = 0; p2 < a.ksplit; ++p2) {
+                const float* pp = pt + static_cast<size_t>(p2) * 2 * BN * kBM;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  gs[i] += __ldcg(pp + static_cast<size_t>(c0 + i) * kBM + fl);
+                  us[i] += __ldcg(pp + static_cast<size_t>(BN + c0 + i) * kBM + fl);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int c = c0 + i;
+                if (c >= te.nrows || te.row0 + c >= a.total_rows) break;
+                const float hv = clamped_swiglu(gs[i], us[i]);
+                const size_t o = static_cast<size_t>(te.row0 + c) * a.I + f;
+                if (kBf16) {
+                  const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+                  const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                  static_cast<__nv_bfloat16*>(a.h0)[o] = hi;
+                  static_cast<__nv_bfloat16*>(a.h1)[o] = lo;
+                } else {
+                  static_cast<__half*>(a.h0)[o] = __float2half_rn(hv);
+                }
+              }
+            }
+          }
+          if (threadIdx.x == kEpiThread0) a.counters[tile] = 0;
+        }
+        epilogue_bar();  // the flags are read before the next unit rewrites them
+        if (Cfg::kAccStages == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       // warp-uniform outcome: tcgen05.ld below is .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.tfull[acc], acc_phase, ab))) break;
       tc_fence_after_sync();
@@ -368,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
   const int total = n_entries_of(a.table, a.dense_rows, BN) * a.mblocks;
+  const int units = total * a.ksplit;  // ksplit > 1 only with the scatter-add epilogue
   const int KB = a.K / kBK;
 
   if (warp == 0) {
@@ -376,7 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int tile = u / a.ksplit, sp = u % a.ksplit;
+        const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
         const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
         const int mb = tile % a.mblocks;
         const bool sh = te.group == a.E;
@@ -384,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ge = sh ? 0 : te.group;
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
         const uint32_t bytes = a.a_rows * kRowBytes + NB * nchunks * kChunkBytes;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab)) {
             ok = false;
             break;
@@ -416,13 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int tile = u / a.ksplit, sp = u % a.ksplit;
+        const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
         const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
         const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
         if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, ab)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + acc * BN;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&sm.full[stage], phase, ab)) {
             ok = false;
             break;
@@ -434,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db1 = sw128_kmajor_desc(st + kATileBytes + Cfg::kBTileBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            umma_f16(d, da + 2 * k, db0 + 2 * k, idesc, (kb | k) != 0);
+            umma_f16(d, da + 2 * k, db0 + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
             if (NB == 2) umma_f16(d, da + 2 * k, db1 + 2 * k, idesc, 1u);
           }
           umma_commit(&sm.empty[stage]);
@@ -459,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int tile = u / a.ksplit;
       const TileEntry te = entry_at(a.table, a.dense_rows, BN, tile / a.mblocks);
       const int mb = tile % a.mblocks;
       // warp-uniform outcome: tcgen05.ld below is .sync.aligned
@@ -532,8 +637,8 @@ cudaError_t gateup_dispatch(const GateUpLaunch& L, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  GateUpArgs a{L.table, L.K, L.I, L.E, L.a_rows, L.total_rows, L.h0, L.h1, L.status,
-               L.budget_ns};
+  GateUpArgs a{L.table, L.K, L.I, L.E, L.a_rows, L.total_rows, L.ksplit > 0 ? L.ksplit : 1,
+               L.partial, L.counters, L.h0, L.h1, L.status, L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
   cfg.blockDim = dim3(kThreads);
@@ -554,8 +659,9 @@ cudaError_t down_dispatch(const DownLaunch& L, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  DownArgs a{L.table, L.dense_rows, L.K, L.N_out, L.mblocks, L.E, L.a_rows, L.total_rows,
-             L.out_rows, L.gather, L.roww, L.bias, L.out, L.status, L.budget_ns};
+  DownArgs a{L.table, L.dense_rows, EPI == kEpiScatterAdd && L.ksplit > 1 ? L.ksplit : 1, L.K,
+             L.N_out, L.mblocks, L.E, L.a_rows, L.total_rows, L.out_rows, L.gather, L.roww,
+             L.bias, L.out, L.status, L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
   cfg.blockDim = dim3(kThreads);

@@ -80,6 +80,9 @@ struct GateUpLaunch {
   int E;             // group id of the shared expert
   int a_rows;        // rows of one weight box (min(128, I))
   int total_rows;    // rows of x_perm / h (stores beyond are dropped)
+  int ksplit;        // K-split units per tile (1 = none); > 1 needs partial + counters
+  float* partial;    // [units][2][BN][128] fp32 partial G/U
+  int* counters;     // [tiles] finished-unit counters, zero between calls
   bool bf16;         // bf16 operands (else fp16)
   void* h0;          // bf16 path: hi plane; fp16 path: h
   void* h1;          // bf16 path: lo plane; fp16 path: null
@@ -104,6 +107,7 @@ struct DownLaunch {
   int a_rows;        // rows of one weight box
   int total_rows;    // rows of the B operand (stores beyond are dropped)
   int out_rows;      // scatter-add: tokens in out (gather ids beyond are dropped)
+  int ksplit;        // K-split units per tile, scatter-add epilogue only (1 = none)
   bool bf16;
   int epilogue;      // DownEpilogue
   const int32_t* gather;

@@ -147,8 +147,11 @@ def test_dense_ffn_bf16(dense_bf16, T):
     x = synthetic.gen_x(wl, T=T)
     out = _dense_run(wl, dev, x)
     sample = np.arange(T) if T <= 16 else np.arange(0, T, max(1, T // 12))
-    assert rel_max_err(out[sample], _dense_ref(wl, w, x[sample])) <= TOL["bf16"]
-    assert np.array_equal(out, _dense_run(wl, dev, x))  # one contribution per element
+    ref = _dense_ref(wl, w, x[sample])
+    assert rel_max_err(out[sample], ref) <= TOL["bf16"]
+    det = _dense_run(wl, dev, x, DET)
+    assert rel_max_err(det[sample], ref) <= TOL["bf16"]
+    assert np.array_equal(det, _dense_run(wl, dev, x, DET))  # one contribution per element
 
 
 def test_dense_ffn_int4_and_accumulate(dense_int4):
