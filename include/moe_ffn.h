@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 2
+#define MOE_FFN_ABI_VERSION 3
 
 /* A cudaStream_t, spelled without the CUDA headers. */
 typedef struct CUstream_st* moe_stream_t;
@@ -128,8 +128,12 @@ moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_route
  *            offsets[E] = top_k*T, offsets[E+1] = (top_k+1)*T
  *   gather   [(top_k+1)*T] int32: token of each row (ascending within a group)
  *   row_of   [T][top_k] int32: row holding (t, j)
- *   x_perm   [(top_k+1)*T][H]: x[gather[r]] -- bf16 for MOE_W_BF16, fp16
- *            (exact conversion of the bf16 input) for MOE_W_INT4_G32.
+ *   x_perm   [(top_k+1)*T][H]: x[gather[r]] -- bf16 for MOE_W_BF16; for
+ *            MOE_W_INT4_G32 fp16 (exact conversion of the bf16 input) in the
+ *            Int4 kernels' operand order: within every aligned group of 8
+ *            columns, position p holds column (0, 4, 1, 5, 2, 6, 3, 7)[p].
+ *            The order is what lets the kernels expand packed codes with
+ *            mask-and-or steps alone; the dot products are unchanged.
  * The grouping that feeds the per-expert matmuls ("ggml_mul_mat_id for
  * gate/up/down", lucebox PR #1, "MoE FFN" section).
  */

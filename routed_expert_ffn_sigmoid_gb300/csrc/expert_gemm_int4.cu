@@ -98,22 +98,24 @@ __device__ __forceinline__ float clamped_swiglu(float g, float u) {
   return gc / (1.0f + expf(-gc)) * uc;
 }
 
-// Eight consecutive codes of one 32-bit word (element 2m in the low nibble of
-// byte m) -> eight fp16 weights (code - 8) * s, as one 16-byte chunk.
-// 0x6400 | n is the fp16 value 1024 + n; subtracting 1032 leaves n - 8 exactly.
+// One 32-bit word of codes (element i of the word in bits 4i .. 4i+3) -> its
+// eight fp16 weights (code - 8) * s as one 16-byte chunk, in the operand order
+// of an aligned 8-element group: (e0, e4), (e1, e5), (e2, e6), (e3, e7).  In
+// that order every pair is one mask-and-or (LOP3), no byte shuffles:
+// (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + e0, 1024 + e4), and
+// (w & 0x00F000F0) | 0x54005400 is (64 + e1, 64 + e5), the nibble sitting four
+// bits up where the ulp of 64 is 1/16.  Subtracting 1032 (or 72) leaves the
+// integer e - 8 exactly; one multiply by the group scale rounds nothing.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t p0 = (__byte_perm(lo, hi, 0x0400) & 0x00FF00FFu) | 0x64006400u;
-  const uint32_t p1 = (__byte_perm(lo, hi, 0x0501) & 0x00FF00FFu) | 0x64006400u;
-  const uint32_t p2 = (__byte_perm(lo, hi, 0x0602) & 0x00FF00FFu) | 0x64006400u;
-  const uint32_t p3 = (__byte_perm(lo, hi, 0x0703) & 0x00FF00FFu) | 0x64006400u;
-  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const uint32_t w8 = w >> 8;
+  const uint32_t p[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                         (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x54005400u};
+  const __half2 off_lo = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 off_hi = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));
   uint32_t r[4];
-  const uint32_t p[4] = {p0, p1, p2, p3};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), off);
+    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), (i & 1) ? off_hi : off_lo);
     v = __hmul2(v, s2);
     r[i] = *reinterpret_cast<const uint32_t*>(&v);
   }
@@ -281,6 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = d >> 7;                 // gate/up: matrix; down: 32-element half
     const int sw = r & 7;                    // 128-byte swizzle phase of this row
     const int m = NA == 2 ? part : 0;
+    constexpr int kHalves = NA == 2 ? 2 : 1; // 32-element groups per sub-block and thread
+    // Byte offsets within the row of the swizzled 16-byte chunks this thread
+    // reads (codes: chunk j = 32 elements = one scale group) and writes (fp16:
+    // chunk c = 8 elements); the same for every stage and slot.
+    uint32_t code_off[kSubPerRaw][kHalves], out_off[kHalves][4];
+#pragma unroll
+    for (int hh = 0; hh < kHalves; ++hh) {
+      const int half = NA == 2 ? hh : part;
+#pragma unroll
+      for (int sb = 0; sb < kSubPerRaw; ++sb) code_off[sb][hh] = ((sb * 2 + half) ^ sw) << 4;
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) out_off[hh][wd] = ((half * 4 + wd) ^ sw) << 4;
+    }
     int rs = 0, os = 0;
     uint32_t rph = 0, oph = 0;
     bool ok = true;
@@ -290,30 +305,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // eight bf16 scales of this row's 256 elements: group j in word j / 2
         const uint4 sv = *reinterpret_cast<const uint4*>(scale_tile(rs, m) + r * 16);
         const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
         const uint8_t* ct = code_tile(rs, m) + r * 128;
-        const int nsub = cmin(kSubPerRaw, KB - rb * kSubPerRaw);
-        for (int sb = 0; sb < nsub; ++sb) {
+        // K is a multiple of the raw stage (256), so every stage holds kSubPerRaw slots
+#pragma unroll
+        for (int sb = 0; sb < kSubPerRaw; ++sb) {
           if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
             ok = false;
             break;
           }
           uint8_t* at = a_tile(os, m) + r * kRowBytes;
 #pragma unroll
-          for (int hh = 0; hh < (NA == 2 ? 2 : 1); ++hh) {
-            const int half = NA == 2 ? hh : part;
-            const int j = sb * 2 + half;       // 16-byte code chunk = 32 elements = one group
-            const uint32_t sbits = (sw4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-            const __half s1 = bf16_bits_to_half(sbits);
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const int shift = (NA == 2 ? hh : part) * 16;  // group 2 sb + half
+            const __half s1 = bf16_bits_to_half((sw4[sb] >> shift) & 0xFFFFu);
             const __half2 s2 = __halves2half2(s1, s1);
-            const uint4 cw = *reinterpret_cast<const uint4*>(ct + ((j ^ sw) << 4));
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-              const int c_out = half * 4 + wd;
-              *reinterpret_cast<uint4*>(at + ((c_out ^ sw) << 4)) = dequant8(words[wd], s2);
-            }
+            const uint4 cw = *reinterpret_cast<const uint4*>(ct + code_off[sb][hh]);
+            *reinterpret_cast<uint4*>(at + out_off[hh][0]) = dequant8(cw.x, s2);
+            *reinterpret_cast<uint4*>(at + out_off[hh][1]) = dequant8(cw.y, s2);
+            *reinterpret_cast<uint4*>(at + out_off[hh][2]) = dequant8(cw.z, s2);
+            *reinterpret_cast<uint4*>(at + out_off[hh][3]) = dequant8(cw.w, s2);
           }
           fence_proxy_async_smem();
           mbar_arrive(&a_full[os]);
@@ -391,6 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
       tc_fence_after_sync();
       const int f = mb * kBM + q * 32 + lane;
+      // column of feature f in the down GEMM's operand order (see dequant8)
+      const int f_op = (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1);
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
       const int n = round16(te.nrows);
       for (int c0 = 0; c0 < n; c0 += 16) {
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float d = __uint_as_float(v0[i]);
               if (NA == 2) {
                 const float hv = clamped_swiglu(d, __uint_as_float(v1[i]));
-                a.h[static_cast<size_t>(rr) * a.N_out + f] = __float2half_rn(hv);
+                a.h[static_cast<size_t>(rr) * a.N_out + f_op] = __float2half_rn(hv);
               } else if (EPI == kEpiScatterAdd) {
                 const int t = a.gather[rr];
                 if (t >= 0 && t < a.out_rows)

@@ -168,15 +168,22 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     for (int c = lane; c < chunks; c += 32) {
       uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
       if (kToFp16) {
-        uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        // exact bf16 -> fp16, the 8 columns stored in the Int4 kernels'
+        // operand order 0, 4, 1, 5, 2, 6, 3, 7
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        float e[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float lo = __uint_as_float(wv[i] << 16);
-          const float hi = __uint_as_float(wv[i] & 0xFFFF0000u);
-          const __half2 h2 = __floats2half2_rn(lo, hi);
-          wv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          e[2 * i] = __uint_as_float(wv[i] << 16);
+          e[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
         }
-        v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h2 = __floats2half2_rn(e[i], e[i + 4]);
+          o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        v = make_uint4(o[0], o[1], o[2], o[3]);
       }
       dst[c] = v;
     }

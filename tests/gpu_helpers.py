@@ -8,6 +8,15 @@ import routed_expert_ffn_sigmoid_gb300 as moe
 
 TOL = {"bf16": 2e-3, "int4": 5e-3}
 
+# moe_permute's Int4 x_perm layout, as the header defines it: position p of
+# every aligned group of 8 columns holds column INT4_COLUMN_ORDER[p].
+INT4_COLUMN_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+
+
+def int4_operand_order(a: np.ndarray) -> np.ndarray:
+    rows, h = a.shape
+    return np.ascontiguousarray(a.reshape(rows, h // 8, 8)[:, :, INT4_COLUMN_ORDER].reshape(rows, h))
+
 
 def torch_mod():
     import torch

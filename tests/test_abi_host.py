@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
     for code in range(6):
         assert moe.moe_status_string(code).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)

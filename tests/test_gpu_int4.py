@@ -15,7 +15,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU container
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import routed_expert_ffn_sigmoid_gb300 as moe  # noqa: E402
-from gpu_helpers import TOL, DeviceLayer, compare_routing, dev_u16  # noqa: E402
+from gpu_helpers import TOL, DeviceLayer, compare_routing, dev_u16, int4_operand_order  # noqa: E402,E501
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +52,7 @@ def test_forward_decode_int4(decode4, T):
     assert rel_max_err(out, _ref(decode4, x)) <= TOL["int4"]
 
 
-def test_permute_int4_converts_rows_to_fp16(decode4):
+def test_permute_int4_converts_rows_to_fp16_operand_order(decode4):
     T = 64
     x = decode4.inp.x[:T]
     z = oracle.router_logits(x, decode4.inp.w_router, decode4.inp.b_router)
@@ -69,7 +69,7 @@ def test_permute_int4_converts_rows_to_fp16(decode4):
     r_off, r_gather, r_row_of = oracle.permute(idx, decode4.wl.E)
     assert np.array_equal(off.cpu().numpy(), r_off)
     assert np.array_equal(gather.cpu().numpy(), r_gather)
-    want = synthetic.bf16_bits_to_f32(x[r_gather]).astype(np.float16)
+    want = int4_operand_order(synthetic.bf16_bits_to_f32(x[r_gather]).astype(np.float16))
     assert np.array_equal(x_perm.cpu().numpy(), want)
 
 
@@ -80,7 +80,8 @@ def test_expert_ffn_int4_rows(decode4):
     idx, _, _ = oracle.topk(z, 8)
     off, gather, row_of = oracle.permute(idx, decode4.wl.E)
     rows = int(off[-1])
-    x_perm = torch.from_numpy(synthetic.bf16_bits_to_f32(x[gather]).astype(np.float16)).cuda()
+    x_perm = torch.from_numpy(
+        int4_operand_order(synthetic.bf16_bits_to_f32(x[gather]).astype(np.float16))).cuda()
     y = torch.empty((rows, decode4.wl.H), dtype=torch.float32, device="cuda")
     ws = decode4.workspace(T)
     moe.moe_expert_ffn(decode4.dims(T), x_perm, torch.from_numpy(off).cuda(), decode4.exw,
