@@ -197,6 +197,8 @@ def parse():
                     help="out += layer(x) (residual add into the output)")
     ap.add_argument("--dense-ffn", type=int, default=0, metavar="I",
                     help="time the dense FFN (intermediate size I) instead of the MoE layer")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager layer calls instead of CUDA graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
@@ -222,6 +224,8 @@ def config_of(wl, world, args=None):
             "expert_weight_bytes": wl.E * expert_bytes(wl),
             "x_batches_cycled": N_BATCHES,
             "l2": "flushed before every step (512 MB write); weights read per step exceed L2",
+            "launch": ("eager layer calls" if args is not None and args.eager else
+                       "CUDA graph replay, one captured layer call per x batch"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -319,27 +323,55 @@ def run_ours(args, wl, rank, world, local):
     if st != moe.MOE_OK:
         raise RuntimeError(moe.moe_status_string(st))
 
-    step_events = [new_events() for _ in range(args.steps)]
+    step_events = [new_events() for _ in range(args.steps)] if args.eager else []
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        time.sleep(0.3)  # let the sampler start before the timed steps
-        for s in range(args.steps):
-            flush.zero_()
-            moe.moe_ffn_forward_timed(dims, xs[s % N_BATCHES], wr, b, exw, shw, out, ws,
-                                      step_events[s][1])
+    if args.eager:
+        with ClockSampler(local) as clk:
+            time.sleep(0.3)  # let the sampler start before the timed steps
+            for s in range(args.steps):
+                flush.zero_()
+                moe.moe_ffn_forward_timed(dims, xs[s % N_BATCHES], wr, b, exw, shw, out, ws,
+                                          step_events[s][1])
+            torch.cuda.synchronize(dev)
+        step_ms = [evs[0].elapsed_time(evs[nst]) for evs, _ in step_events]
+        stage_ms = [[evs[i].elapsed_time(evs[i + 1]) for evs, _ in step_events]
+                    for i in range(nst)]
+    else:
+        # One graph per x batch: the layer call (all its kernels and stage
+        # events) captured once, replayed every step; the L2 flush runs
+        # between replays, outside the graphs.
+        graphs = []
+        cap = torch.cuda.Stream(dev)
+        for bi in range(N_BATCHES):
+            evs, se = new_events()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                moe.moe_ffn_forward_timed(dims, xs[bi], wr, b, exw, shw, out, ws, se)
+            graphs.append((g, evs))
+        for s in range(args.warmup):
+            graphs[s % N_BATCHES][0].replay()
         torch.cuda.synchronize(dev)
+        step_ms, stage_ms = [], [[] for _ in range(nst)]
+        with ClockSampler(local) as clk:
+            time.sleep(0.3)
+            for s in range(args.steps):
+                flush.zero_()
+                g, evs = graphs[s % N_BATCHES]
+                g.replay()
+                # the graph's events are read before the graph runs again
+                torch.cuda.synchronize(dev)
+                step_ms.append(evs[0].elapsed_time(evs[nst]))
+                for i in range(nst):
+                    stage_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     st = moe.moe_workspace_status(ws)
     if st != moe.MOE_OK:
         raise RuntimeError(moe.moe_status_string(st))
-
-    step_ms = [evs[0].elapsed_time(evs[nst]) for evs, _ in step_events]
-    stage_ms = [[evs[i].elapsed_time(evs[i + 1]) for evs, _ in step_events] for i in range(nst)]
     value, ms_per_step = replicas.job_throughput(sum(step_ms), wl.T, args.steps, world, dev)
 
     # end to end through the C ABI with host buffers: H2D x, layer, D2H out
@@ -457,12 +489,26 @@ def run_dense(args, rank, world, local):
            for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
+    if not args.eager:  # one captured call per x batch, replayed
+        graphs = []
+        cap = torch.cuda.Stream(dev)
+        for bi in range(N_BATCHES):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                moe.moe_dense_ffn(dims, xs[bi], weights, out, ws)
+            graphs.append(g)
+        for s_ in range(args.warmup):
+            graphs[s_ % N_BATCHES].replay()
+        torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         for s_ in range(args.steps):
             flush.zero_()
             evs[s_][0].record(stream)
-            moe.moe_dense_ffn(dims, xs[s_ % N_BATCHES], weights, out, ws)
+            if args.eager:
+                moe.moe_dense_ffn(dims, xs[s_ % N_BATCHES], weights, out, ws)
+            else:
+                graphs[s_ % N_BATCHES].replay()
             evs[s_][1].record(stream)
         torch.cuda.synchronize(dev)
     st = moe.moe_workspace_status(ws)
@@ -494,7 +540,9 @@ def run_dense(args, rank, world, local):
                      "int4 weights dequantised to fp16, fp32 accumulate",
             "data": "synthetic (seeded generator; random-init weights)",
             "config": {"workload": f"dense FFN T={wl.T} H={wl.H} I={I} {wl.fmt} weights",
-                       "l2": "flushed before every step (512 MB write)"},
+                       "l2": "flushed before every step (512 MB write)",
+                       "launch": "eager layer calls" if args.eager else
+                                 "CUDA graph replay, one captured call per x batch"},
             "roofline": roof, "gbs": gbs, "tflops": tflops,
             # dense-rows table, gate/up, down (+ the fp16 conversion of x for Int4)
             "gpu_launches": (3 + (1 if wl.fmt != "bf16" else 0)) * args.steps,

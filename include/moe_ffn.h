@@ -187,10 +187,12 @@ moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_route
 /*
  * Stage boundaries of moe_ffn_forward_timed: ev[i] is recorded on `stream`
  * before stage i, ev[MOE_STAGE_COUNT] after the last one.  Stages:
- *   0 router logits + top-k (for T <= 128 the top-k runs in stage 1, fused
- *     with the permutation)     1 permutation (count, scan, scatter, gather)
+ *   0 router logits + top-k      1 permutation (count, scan, scatter, gather;
+ *                                  one kernel + gather for T <= 128)
  *   2 grouped gate/up + SwiGLU   3 grouped down + weighted scatter-add
  * Each ev[i] is a cudaEvent_t created by the caller (NULL entries are skipped).
+ * When `stream` is being captured into a CUDA graph the records are captured
+ * as external event nodes, so each replay of the graph records them again.
  */
 #define MOE_STAGE_COUNT 4
 typedef struct moe_stage_events {

@@ -81,7 +81,9 @@ Layout layout_of(const moe_dims& d) {
     o = align_up(o + bytes);
     return at;
   };
-  L.z = take(T * E * 4);
+  // logits [T][E], or below the tensor-core router's size the partial
+  // logits of every reduction slice [slices][T][E]
+  L.z = take((d.T < kRouterTcMinTokens ? static_cast<size_t>(router_slices(d.H)) : 1) * T * E * 4);
   L.idx = take(T * k * 4);
   L.w = take(T * k * 4);
   L.blockcnt = take(nblk * E * 4);
@@ -252,13 +254,23 @@ moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes, Ws* out) {
 
 // ------------------------------------------------------------ stages
 
-// Router logits into the workspace (tensor cores from kRouterTcMinTokens
-// tokens, CUDA cores below).
-moe_status run_logits(const moe_dims& d, const void* x, const void* w_router, const float* b,
-                      const Ws& ws, cudaStream_t s) {
+// Router logits and top-k.  From kRouterTcMinTokens tokens the logits come
+// from the tensor cores (bias in the epilogue) and a warp per token selects;
+// below, partial logits per reduction slice spread the router matrix over
+// all SMs and a warp per token adds the slices, the bias and selects.
+moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
+                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
   float* z = ws.at<float>(ws.L.z);
+  if (d.T < kRouterTcMinTokens) {
+    if (launch_router_partials(static_cast<const uint16_t*>(x),
+                               static_cast<const uint16_t*>(w_router), z, d.T, d.H, d.E,
+                               s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return from_cuda(
+        launch_router_reduce_topk(z, b, d.T, d.H, d.E, d.top_k, idx, w, nullptr, s));
+  }
   cudaError_t e;
-  if (d.T >= kRouterTcMinTokens) {
+  {
     DownLaunch L{};
     if (!encode_weights(&L.tm_a, w_router, true, d.H, d.E, 1) ||
         !encode_kmajor(&L.tm_b0, x, true, d.H, d.T, 1, 16))
@@ -286,18 +298,9 @@ moe_status run_logits(const moe_dims& d, const void* x, const void* w_router, co
     const int tiles = ((d.T + 127) / 128) * L.mblocks;
     L.grid = tiles < sm_count() ? tiles : sm_count();
     e = launch_down(L, s);
-  } else {
-    e = launch_router_logits_simt(static_cast<const uint16_t*>(x),
-                                  static_cast<const uint16_t*>(w_router), b, z, d.T, d.H, d.E, s);
   }
-  return from_cuda(e);
-}
-
-moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
-                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
-  const moe_status st = run_logits(d, x, w_router, b, ws, s);
-  if (st != MOE_OK) return st;
-  return from_cuda(launch_topk(ws.at<float>(ws.L.z), d.T, d.E, d.top_k, idx, w, s));
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return from_cuda(launch_topk(z, d.T, d.E, d.top_k, idx, w, s));
 }
 
 moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, const void* x,
@@ -318,8 +321,15 @@ moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, co
 }
 
 // Grouped gate/up + down over the permuted rows described by `table`.
+// Under stream capture the records become event nodes of the graph, so that
+// every replay times its own stages.
 void record(const moe_stage_events* ev, int i, cudaStream_t s) {
-  if (ev && ev->ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev->ev[i]), s);
+  if (!ev || !ev->ev[i]) return;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cap);
+  cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev->ev[i]), s,
+                           cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                : cudaEventRecordDefault);
 }
 
 moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* table,
@@ -548,10 +558,10 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   float* zero_out = (det || accumulate) ? nullptr : out;
   record(ev, 0, s);
   if (d->T <= kSmallT) {
-    // decode sizes: logits, then one CTA for top-k + the whole permutation
-    if ((st = run_logits(*d, x, w_router, b_router, w, s)) != MOE_OK) return st;
+    // decode sizes: router, then one CTA for the whole permutation
+    if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
     record(ev, 1, s);
-    if (launch_route_small(w.at<float>(L.z), d->T, d->E, d->top_k, pick_bn(d->T), idx, wts,
+    if (launch_route_small(nullptr, d->T, d->E, d->top_k, pick_bn(d->T), idx, wts,
                            w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of), roww,
                            table, s) != cudaSuccess)
       return MOE_ERR_CUDA;

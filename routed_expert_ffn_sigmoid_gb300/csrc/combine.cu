@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   __shared__ int rows[kMaxTopK + 1];
   __shared__ float wt[kMaxTopK];
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
     if (threadIdx.x < k) {

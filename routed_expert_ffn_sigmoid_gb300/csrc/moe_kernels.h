@@ -29,6 +29,15 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_route
                                       float* z, int T, int H, int E, cudaStream_t s);
 
 // Per token: top_k of z (ties to the lower index), sigmoid, renormalise.
+// Decode-size router: partial logits per reduction slice of kRouterSliceK
+// elements, part [slices][T][E] fp32, then per token the slice sum in slice
+// order + bias and the top-k (z [T][E] also written when z != nullptr).
+constexpr int kRouterSliceK = 256;
+inline int router_slices(int H) { return (H + kRouterSliceK - 1) / kRouterSliceK; }
+cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, float* part,
+                                  int T, int H, int E, cudaStream_t s);
+cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
+                                      int k, int32_t* idx, float* w, float* z, cudaStream_t s);
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
 
@@ -50,8 +59,9 @@ cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
                                bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
                                cudaStream_t s);
-// T <= kSmallT: top-k, histogram, offsets, stable ranks, gather / row_of /
-// row weights and the tile table in one CTA.
+// T <= kSmallT: top-k (from the logits z, or z == nullptr: read from idx / w),
+// histogram, offsets, stable ranks, gather / row_of / row weights and the
+// tile table in one CTA.
 cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
                                float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
                                float* roww, int32_t* table, cudaStream_t s);

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ blockcnt) {
   __shared__ int cnt[kMaxE];
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * kPermTokBlock;
@@ -39,7 +40,6 @@ __global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restri
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
-  pdl_launch_dependents();
 }
 
 // One CTA of 1024 threads.
@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
   __shared__ int n_entries;
   __shared__ int total_rows;
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   const int nblk = (T + kPermTokBlock - 1) / kPermTokBlock;
   // per expert: running sum over blocks (becomes the block-relative base)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -95,7 +96,6 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
     }
   }
   if (threadIdx.x == 0) table[0] = n_entries;
-  pdl_launch_dependents();
 }
 
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __restrict__ idx,
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
                                                            float* __restrict__ roww) {
   __shared__ uint32_t bits[kMaxE][kWordsPerBlock];
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   for (int i = threadIdx.x; i < E * kWordsPerBlock; i += blockDim.x) (&bits[0][0])[i] = 0u;
   __syncthreads();
   const int t0 = blockIdx.x * kPermTokBlock;
@@ -137,7 +138,6 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
     gather[r] = t0 + tl;
     if (roww) roww[r] = 1.0f;
   }
-  pdl_launch_dependents();
 }
 
 // One warp per row, grid-stride.  H is a multiple of 128, so a row is a whole
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           float4* __restrict__ zero_out,
                                                           size_t zero_n4) {
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   if (zero_out) {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_n4;
@@ -188,7 +189,6 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
       dst[c] = v;
     }
   }
-  pdl_launch_dependents();
 }
 
 // Tile table from an offsets array (E+2 entries), one CTA.  Offsets are
@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
   __shared__ int ntile[kMaxE + 1];
   __shared__ int n_entries;
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   for (int g = threadIdx.x; g <= E; g += blockDim.x) {
     const int a = min(max(offsets[g], 0), rows);
     const int b = min(max(offsets[g + 1], a), rows);
@@ -227,11 +228,11 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
     }
   }
   if (threadIdx.x == 0) table[0] = min(n_entries, capacity);
-  pdl_launch_dependents();
 }
 
-// Decode-size routing in one CTA (T <= kSmallT tokens): per-token top-k,
-// expert histogram, exclusive offsets (shared expert appended as group E),
+// Decode-size routing in one CTA (T <= kSmallT tokens): per-token top-k of
+// the logits z (or, with z null, the selection already in idx / w), expert
+// histogram, exclusive offsets (shared expert appended as group E),
 // stable ranks from per-expert token bitmaps, gather / row_of / row weights
 // and the tile table -- the work of the top-k, count, scan and scatter
 // kernels without three launches in between.
@@ -248,16 +249,24 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   for (int g = threadIdx.x; g <= E; g += blockDim.x) cnt[g] = 0;
   for (int i = threadIdx.x; i < E * (kSmallT / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = warp; t < T; t += kSmallThreads / 32) {
-    int e;
-    float wv;
-    warp_topk(z + static_cast<size_t>(t) * E, E, k, &e, &wv);
-    if (lane < k) {
-      s_idx[t * k + lane] = e;
-      s_w[t * k + lane] = wv;
-      idx_out[t * k + lane] = e;
-      w_out[t * k + lane] = wv;
+  if (z) {
+    for (int t = warp; t < T; t += kSmallThreads / 32) {
+      int e;
+      float wv;
+      warp_topk(z + static_cast<size_t>(t) * E, E, k, &e, &wv);
+      if (lane < k) {
+        s_idx[t * k + lane] = e;
+        s_w[t * k + lane] = wv;
+        idx_out[t * k + lane] = e;
+        w_out[t * k + lane] = wv;
+      }
+    }
+  } else {  // the selection is already in idx / w
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+      s_idx[i] = idx_out[i];
+      s_w[i] = w_out[i];
     }
   }
   __syncthreads();
@@ -303,7 +312,6 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     }
   }
   if (threadIdx.x == 0) table[0] = n_entries;
-  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(256) dense_rows_kernel(int T, int BN, int32_t*
                                                          float* __restrict__ roww,
                                                          int32_t* __restrict__ table) {
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   const int n = (T + BN - 1) / BN;
   TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T || i < n; i += gridDim.x * blockDim.x) {
@@ -380,7 +389,6 @@ __global__ void __launch_bounds__(256) dense_rows_kernel(int T, int BN, int32_t*
     }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) table[0] = n;
-  pdl_launch_dependents();
 }
 
 }  // namespace

@@ -27,16 +27,11 @@ constexpr int kTopkVPL = kMaxE / 32;  // logits held per lane
 // Lane L holds experts L, L+32, ...; each round takes the warp maximum of the
 // 64-bit key (score key << 32 | ~e): the larger score wins and an exact tie
 // goes to the lower expert index.  Lane j < k ends with slot j: *e_out, and
-// *w_out = sigmoid(z_j) / sum of the k sigmoids.
-__device__ __forceinline__ void warp_topk(const float* __restrict__ zr, int E, int k, int* e_out,
-                                          float* w_out) {
+// *w_out = sigmoid(z_j) / sum of the k sigmoids.  keys[i] = float_key(z) of
+// expert i * 32 + lane.
+__device__ __forceinline__ void warp_topk_keys(const uint32_t (&keys)[kTopkVPL], int E, int k,
+                                               int* e_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  uint32_t keys[kTopkVPL];
-#pragma unroll
-  for (int i = 0; i < kTopkVPL; ++i) {
-    const int e = i * 32 + lane;
-    keys[i] = e < E ? float_key(zr[e]) : 0u;
-  }
   uint32_t taken = 0;
   int my_e = 0;
   float my_z = 0.f;
@@ -71,6 +66,19 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ zr, int E, i
   *w_out = s / sum;
 }
 
+// The same selection from a row of E logits in memory.
+__device__ __forceinline__ void warp_topk(const float* __restrict__ zr, int E, int k, int* e_out,
+                                          float* w_out) {
+  const int lane = threadIdx.x & 31;
+  uint32_t keys[kTopkVPL];
+#pragma unroll
+  for (int i = 0; i < kTopkVPL; ++i) {
+    const int e = i * 32 + lane;
+    keys[i] = e < E ? float_key(zr[e]) : 0u;
+  }
+  warp_topk_keys(keys, E, k, e_out, w_out);
+}
+
 // Exclusive scan of n values in shared memory by warp 0; *total gets the sum.
 // Other threads return at once; the caller synchronises.
 __device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) {
@@ -94,7 +102,10 @@ __device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) 
 
 // Launch helper: programmatic stream serialization lets a kernel begin while
 // its predecessor drains; every kernel launched this way calls pdl_wait()
-// before it touches data a predecessor produced.
+// before it touches data a predecessor produced.  The routing kernels call
+// pdl_launch_dependents() right after that wait: the next grid's CTAs are
+// then scheduled while this one runs (hiding their launch), and still wait
+// in their own pdl_wait() for this grid to complete.
 template <typename Kern, typename... Args>
 cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args... args) {

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(128) router_logits_simt_kernel(const uint16_t*
                                                                  int H, int E) {
   extern __shared__ uint4 xs[];  // [kRouterTokTile][H / 8]
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   const int chunks = H / 8;
   const int t0 = blockIdx.y * kRouterTokTile;
   const int nt = min(kRouterTokTile, T - t0);
@@ -88,7 +89,176 @@ __global__ void __launch_bounds__(128) router_logits_simt_kernel(const uint16_t*
       if (lane == 0 && t < nt) z[static_cast<size_t>(t0 + t) * E + e] = v + bias;
     }
   }
-  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------- decode-size router
+// Logits for up to a few hundred tokens are a GEMV-like product too small for
+// the tensor-core pipeline to fill the GPU.  The reduction dimension is cut
+// into slices so that every SM streams a slice of the router matrix at once:
+// CTA (expert block, slice) stages its 32 router rows and the token rows of
+// its slice as fp32 in shared memory (all global loads issued before the
+// first use) and writes partial logits part[slice][t][e]; a second kernel
+// adds the slices in slice order (a fixed order: the logits are the same on
+// every run), adds the bias and selects the top-k, one warp per token.
+
+constexpr int kPartExperts = 32;                 // router rows per CTA
+constexpr int kPartTok = 64;                     // token rows per pass
+constexpr int kPartRow = kRouterSliceK + 4;      // padded fp32 row: lanes on distinct banks
+constexpr int kPartThreads = 256;                // warp w: experts 4w .. 4w + 3
+constexpr int kPartWLoads = kPartExperts * (kRouterSliceK / 8) / kPartThreads;  // 4
+constexpr int kPartXLoads = kPartTok * (kRouterSliceK / 8) / kPartThreads;      // 8
+constexpr size_t kPartSmem = static_cast<size_t>(kPartTok + kPartExperts) * kPartRow * 4;
+
+__device__ __forceinline__ void store_f32x8(float* dst, const uint4& v) {
+  float f[8];
+  bf16x8_to_f32(v, f);
+  reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// acc[a][e] = sum over the slice of x[lane + 32 a][k] * w[4 warp + e][k] for
+// the first NR token rows of the lane (rows left out stay 0).
+template <int NR>
+__device__ __forceinline__ void partial_dot(const float* xs, const float* wsm, int lane, int warp,
+                                            float (&acc)[2][4]) {
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+  const float* xa = xs + lane * kPartRow;
+  const float* xb = xs + (lane + 32) * kPartRow;
+  const float* wb = wsm + (warp * 4) * kPartRow;
+#pragma unroll 4
+  for (int kk = 0; kk < kRouterSliceK; kk += 4) {
+    float4 a4[2];
+    a4[0] = *reinterpret_cast<const float4*>(xa + kk);
+    if (NR == 2) a4[1] = *reinterpret_cast<const float4*>(xb + kk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 b4 = *reinterpret_cast<const float4*>(wb + e * kPartRow + kk);
+#pragma unroll
+      for (int a = 0; a < NR; ++a) {
+        acc[a][e] = fmaf(a4[a].x, b4.x, acc[a][e]);
+        acc[a][e] = fmaf(a4[a].y, b4.y, acc[a][e]);
+        acc[a][e] = fmaf(a4[a].z, b4.z, acc[a][e]);
+        acc[a][e] = fmaf(a4[a].w, b4.w, acc[a][e]);
+      }
+    }
+  }
+}
+
+// grid (ceil(E / 32), ceil(H / kRouterSliceK)), kPartThreads threads.
+__global__ void __launch_bounds__(kPartThreads) router_partial_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, int T, int H, int E,
+    float* __restrict__ part) {
+  extern __shared__ float4 smem_f4[];
+  float* xs = reinterpret_cast<float*>(smem_f4);  // [kPartTok][kPartRow]
+  float* wsm = xs + kPartTok * kPartRow;          // [kPartExperts][kPartRow]
+  const int e0 = blockIdx.x * kPartExperts;
+  const int k0 = blockIdx.y * kRouterSliceK;
+  const int nk = min(kRouterSliceK, H - k0);  // H % 8 == 0: whole 8-element chunks
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kChunksPerRow = kRouterSliceK / 8;
+  pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  // router rows of the block (zero past E and past H)
+  uint4 wv[kPartWLoads];
+#pragma unroll
+  for (int j = 0; j < kPartWLoads; ++j) {
+    const int i = threadIdx.x + j * kPartThreads, r = i / kChunksPerRow, c = i % kChunksPerRow;
+    wv[j] = (e0 + r < E && c * 8 < nk)
+                ? __ldg(reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e0 + r) * H + k0) + c)
+                : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int t0 = 0; t0 < T; t0 += kPartTok) {
+    const int nt = min(kPartTok, T - t0);
+    uint4 xv[kPartXLoads];
+#pragma unroll
+    for (int j = 0; j < kPartXLoads; ++j) {
+      const int i = threadIdx.x + j * kPartThreads, r = i / kChunksPerRow, c = i % kChunksPerRow;
+      xv[j] = (r < nt && c * 8 < nk)
+                  ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + r) * H + k0) + c)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (t0 == 0) {
+#pragma unroll
+      for (int j = 0; j < kPartWLoads; ++j) {
+        const int i = threadIdx.x + j * kPartThreads;
+        store_f32x8(wsm + (i / kChunksPerRow) * kPartRow + (i % kChunksPerRow) * 8, wv[j]);
+      }
+    } else {
+      __syncthreads();  // the previous pass has read xs
+    }
+#pragma unroll
+    for (int j = 0; j < kPartXLoads; ++j) {
+      const int i = threadIdx.x + j * kPartThreads;
+      store_f32x8(xs + (i / kChunksPerRow) * kPartRow + (i % kChunksPerRow) * 8, xv[j]);
+    }
+    __syncthreads();
+    // lane: tokens lane and lane + 32; warp: experts 4 warp .. 4 warp + 3
+    float acc[2][4];
+    if (nt > 32)
+      partial_dot<2>(xs, wsm, lane, warp, acc);
+    else
+      partial_dot<1>(xs, wsm, lane, warp, acc);
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int t = lane + 32 * a;
+      if (t < nt) {
+        float* dst = part + (static_cast<size_t>(blockIdx.y) * T + t0 + t) * E;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e0 + warp * 4 + e < E) dst[e0 + warp * 4 + e] = acc[a][e];
+      }
+    }
+  }
+}
+
+// One CTA per token, one thread per expert: z = (sum over slices, in slice
+// order) + bias, with every slice's load in flight at once; warp 0 then
+// selects the top-k from shared memory.  Writes idx / w, and z itself when
+// z_out is given.
+constexpr int kReduceBatch = 16;  // slice loads in flight per thread
+
+__global__ void __launch_bounds__(kMaxE) router_reduce_topk_kernel(
+    const float* __restrict__ part, const float* __restrict__ b, int T, int E, int slices, int k,
+    int32_t* __restrict__ idx, float* __restrict__ w, float* __restrict__ z_out) {
+  __shared__ uint32_t keys_s[kMaxE];
+  pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  const int t = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+    for (int s0 = 0; s0 < slices; s0 += kReduceBatch) {
+      float v[kReduceBatch];
+#pragma unroll
+      for (int j = 0; j < kReduceBatch; ++j)
+        v[j] = s0 + j < slices ? part[(static_cast<size_t>(s0 + j) * T + t) * E + e] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kReduceBatch; ++j)
+        if (s0 + j < slices) acc += v[j];
+    }
+    const float zv = acc + b[e];
+    keys_s[e] = float_key(zv);
+    if (z_out) z_out[static_cast<size_t>(t) * E + e] = zv;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t keys[kTopkVPL];
+#pragma unroll
+    for (int i = 0; i < kTopkVPL; ++i) {
+      const int e = i * 32 + lane;
+      keys[i] = e < E ? keys_s[e] : 0u;
+    }
+    int e;
+    float wv;
+    warp_topk_keys(keys, E, k, &e, &wv);
+    if (lane < k) {
+      idx[static_cast<size_t>(t) * k + lane] = e;
+      w[static_cast<size_t>(t) * k + lane] = wv;
+    }
+  }
 }
 
 // One warp per token: top-k, sigmoid, renormalisation.
@@ -96,6 +266,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ z, 
                                                    int k, int32_t* __restrict__ idx,
                                                    float* __restrict__ w) {
   pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t < T) {
@@ -107,7 +278,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ z, 
       w[static_cast<size_t>(t) * k + lane] = wv;
     }
   }
-  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -123,6 +293,26 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_route
   const dim3 grid((E + kRouterWarps - 1) / kRouterWarps, (T + kRouterTokTile - 1) / kRouterTokTile);
   return launch_pdl(router_logits_simt_kernel, grid, dim3(32 * kRouterWarps), smem, s, x,
                     w_router, b, z, T, H, E);
+}
+
+cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, float* part,
+                                  int T, int H, int E, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(router_partial_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPartSmem));
+  if (err != cudaSuccess) return err;
+  const dim3 grid((E + kPartExperts - 1) / kPartExperts, router_slices(H));
+  return launch_pdl(router_partial_kernel, grid, dim3(kPartThreads), kPartSmem, s, x, w_router,
+                    T, H, E, part);
+}
+
+cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
+                                      int k, int32_t* idx, float* w, float* z, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int threads = ((E + 31) / 32) * 32;  // E <= kMaxE
+  return launch_pdl(router_reduce_topk_kernel, dim3(T), dim3(threads), 0, s, part, b, T, E,
+                    router_slices(H), k, idx, w, z);
 }
 
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,

@@ -169,3 +169,29 @@ def test_dense_ffn_int4_and_accumulate(dense_int4, T):
     resid = np.random.default_rng(3).standard_normal((T, wl.H)).astype(np.float32)
     acc = _dense_run(wl, dev, x, ACC, out_init=resid)[sample]
     assert rel_max_err(acc - resid[sample].astype(np.float64), ref) <= TOL["int4"]
+
+
+# ------------------------------------------------------------------ CUDA graph capture
+
+@pytest.mark.parametrize("T", [1, 64, 300])
+def test_forward_replays_from_a_cuda_graph(decode, T):
+    """moe_ffn_forward makes no synchronising call, so a caller can capture it
+    into a CUDA graph; replays give the eager result bit for bit (DET mode)."""
+    x = decode.inp.x[:T] if T <= decode.wl.T else gapped_x(
+        decode.wl, decode.inp.w_router, decode.inp.b_router, T=T)[0]
+    wl = decode.wl
+    dims = moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, DET)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    xd = dev_u16(x)
+    out = torch.empty((T, wl.H), dtype=torch.float32, device="cuda")
+    moe.moe_ffn_forward(dims, xd, decode.wr, decode.b, decode.exw, decode.shw, out, ws)
+    eager = out.cpu().numpy()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        moe.moe_ffn_forward(dims, xd, decode.wr, decode.b, decode.exw, decode.shw, out, ws)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), eager)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
