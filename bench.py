@@ -438,15 +438,21 @@ def run_ours(args, wl, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
             # T <= 128: logits, one-CTA routing, gather, gate/up, down; larger T:
-            # logits, top-k, count, scan, scatter, gather, gate/up, down;
-            # + the fixed-order combination in the deterministic mode
-            "gpu_launches": ((5 if wl.T <= 128 else 8) + (1 if args.deterministic else 0))
-                            * args.steps,
+            "gpu_launches": layer_launches(wl.T, args.deterministic) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def layer_launches(T, deterministic):
+    """Kernels one moe_ffn_forward launches.  T <= 128: router partial logits,
+    slice sum + top-k, one-CTA permutation, gather, gate/up, down.  Larger T:
+    logits (partial sums below 256 tokens, tensor cores from 256), top-k,
+    count, scan, scatter, gather, gate/up, down.  Deterministic mode adds the
+    fixed-order combination."""
+    return (6 if T <= 128 else 8) + (1 if deterministic else 0)
 
 
 def run_dense(args, rank, world, local):
