@@ -438,7 +438,7 @@ def run_ours(args, wl, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
             # T <= 128: logits, one-CTA routing, gather, gate/up, down; larger T:
-            "gpu_launches": layer_launches(wl.T, args.deterministic) * args.steps,
+            "gpu_launches": layer_launches(wl.T, args.deterministic, wl.fmt) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -446,13 +446,16 @@ def run_ours(args, wl, rank, world, local):
         torch.distributed.destroy_process_group()
 
 
-def layer_launches(T, deterministic):
+def layer_launches(T, deterministic, fmt="bf16"):
     """Kernels one moe_ffn_forward launches.  T <= 128: router partial logits,
-    slice sum + top-k, one-CTA permutation, gather, gate/up, down.  Larger T:
-    logits (partial sums below 256 tokens, tensor cores from 256), top-k,
-    count, scan, scatter, gather, gate/up, down.  Deterministic mode adds the
-    fixed-order combination."""
-    return (6 if T <= 128 else 8) + (1 if deterministic else 0)
+    slice sum + top-k, one-CTA permutation, gate/up, down.  Larger T: logits
+    (partial sums below 256 tokens, tensor cores from 256), top-k, count,
+    scan, scatter, gate/up, down.  The bf16 gate/up GEMM gathers the token rows
+    from x itself up to 8 tokens; above, and always for Int4, one more kernel
+    writes x_perm.  Deterministic mode adds the fixed-order combination."""
+    gathers_itself = fmt == "bf16" and T <= 8
+    return ((5 if T <= 128 else 7) + (0 if gathers_itself else 1)
+            + (1 if deterministic else 0))
 
 
 def run_dense(args, rank, world, local):

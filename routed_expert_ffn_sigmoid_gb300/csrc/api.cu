@@ -18,6 +18,7 @@ namespace {
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;        // status word + reserved
 constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many tokens
+constexpr int kGatherFromXTokens = 8;       // bf16 gate/up gathers its token rows from x up to this
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -258,13 +259,16 @@ moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes, Ws* out) {
 // from the tensor cores (bias in the epilogue) and a warp per token selects;
 // below, partial logits per reduction slice spread the router matrix over
 // all SMs and a warp per token adds the slices, the bias and selects.
+// With zero_out, the router's kernels also clear out [T][H].
 moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
-                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s) {
+                      int32_t* idx, float* w, const Ws& ws, cudaStream_t s,
+                      float* zero_out = nullptr) {
   float* z = ws.at<float>(ws.L.z);
+  const size_t zero_n = zero_out ? static_cast<size_t>(d.T) * d.H : 0;
   if (d.T < kRouterTcMinTokens) {
     if (launch_router_partials(static_cast<const uint16_t*>(x),
                                static_cast<const uint16_t*>(w_router), z, d.T, d.H, d.E,
-                               s) != cudaSuccess)
+                               zero_out, zero_n, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     return from_cuda(
         launch_router_reduce_topk(z, b, d.T, d.H, d.E, d.top_k, idx, w, nullptr, s));
@@ -300,27 +304,28 @@ moe_status run_router(const moe_dims& d, const void* x, const void* w_router, co
     e = launch_down(L, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return from_cuda(launch_topk(z, d.T, d.E, d.top_k, idx, w, s));
+  return from_cuda(launch_topk(z, d.T, d.E, d.top_k, idx, w, s, zero_out, zero_n));
 }
 
+// materialise: also write x_perm (and clear zero_out) with the gather kernel;
+// the fused bf16 path leaves it out, its GEMMs read the rows from x.
 moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, const void* x,
                        int32_t* offsets, int32_t* gather, int32_t* row_of, float* roww,
                        void* x_perm, int32_t* table, const Ws& ws, cudaStream_t s,
-                       float* zero_out = nullptr) {
+                       float* zero_out = nullptr, bool materialise = true) {
   int32_t* blockcnt = ws.at<int32_t>(ws.L.blockcnt);
   cudaError_t e = launch_perm_count(idx, d.T, d.E, d.top_k, blockcnt, s);
   if (e == cudaSuccess)
     e = launch_perm_scan(blockcnt, d.T, d.E, d.top_k, offsets, table, pick_bn(d.T), s);
   if (e == cudaSuccess)
     e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && materialise)
     e = launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(d), d.H, d.T,
                            d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
                            zero_out ? static_cast<size_t>(d.T) * d.H : 0, s);
   return from_cuda(e);
 }
 
-// Grouped gate/up + down over the permuted rows described by `table`.
 // Under stream capture the records become event nodes of the graph, so that
 // every replay times its own stages.
 void record(const moe_stage_events* ev, int i, cudaStream_t s) {
@@ -332,10 +337,15 @@ void record(const moe_stage_events* ev, int i, cudaStream_t s) {
                                                                 : cudaEventRecordDefault);
 }
 
+// Grouped gate/up + down over the permuted rows described by `table`.
+// Token rows: x_perm [rows][H] (xrows null), or with xrows (bf16 weights,
+// the weights-as-M kernels) the gate/up GEMM reads row r as x[xrows[r]]
+// straight from x = `x_perm` [T][H].
 moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* table,
                        const moe_weights* ex, const moe_weights* sh, int epilogue,
                        const int32_t* gather, const float* roww, float* out, const Ws& ws,
-                       cudaStream_t s, const moe_stage_events* ev = nullptr) {
+                       cudaStream_t s, const moe_stage_events* ev = nullptr,
+                       const int32_t* xrows = nullptr) {
   const int rows = rows_of(d);
   const int BN = pick_bn(d.T);
   const int nsm = sm_count();
@@ -404,6 +414,7 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
   if (BN == 128 && d.I % 128 == 0 && d.H % 256 == 0) {
     // token-major kernels: tiles of up to 128 rows of one group
     TmLaunch G{};
+    if (xrows) return MOE_ERR_UNSUPPORTED;  // token-major tiles read x_perm
     if (!encode_kmajor(&G.tm_a[0], x_perm, true, d.H, rows, 1, 128) ||
         !encode_weights(&G.tm_b[0], ex->gate, true, d.H, d.I, d.E, 128) ||
         !encode_weights(&G.tm_b[1], ex->up, true, d.H, d.I, d.E, 128) ||
@@ -462,9 +473,11 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
       !encode_weights(&G.tm_up, ex->up, bf16, d.H, d.I, d.E) ||
       !encode_weights(&G.tm_sgate, sh->gate, bf16, d.H, d.I, 1) ||
       !encode_weights(&G.tm_sup, sh->up, bf16, d.H, d.I, 1) ||
-      !encode_kmajor(&G.tm_x, x_perm, bf16, d.H, rows, 1, 16))
+      !(xrows ? encode_kmajor(&G.tm_x, x_perm, bf16, d.H, d.T, 1, 1)
+              : encode_kmajor(&G.tm_x, x_perm, bf16, d.H, rows, 1, 16)))
     return MOE_ERR_CUDA;
   G.table = table;
+  G.xrows = xrows;
   G.BN = BN;
   G.K = d.H;
   G.I = d.I;
@@ -554,35 +567,49 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   void* x_perm = w.at<void>(L.x_perm);
   const bool det = (d->flags & MOE_FLAG_DETERMINISTIC) != 0;
   const bool accumulate = (d->flags & MOE_FLAG_ACCUMULATE) != 0;
-  // out is cleared by the gather kernel only when the down epilogue adds into it
+  // out is cleared (by the router kernels, or for Int4 by the gather that
+  // converts x) only when the down epilogue adds into it
   float* zero_out = (det || accumulate) ? nullptr : out;
+  // bf16 weights, up to kGatherFromXTokens tokens: the gate/up GEMM gathers
+  // each token row straight from x (tile::gather4), so the permuted copy of x
+  // and its kernel drop out.  The gathers cost the copy engine about 3 % of
+  // the gate/up time on every stage, more than the copy kernel they replace
+  // once T grows (measured), so larger T reads a materialised x_perm; Int4
+  // always needs the fp16 copy in its operand order.
+  const bool int4 = d->fmt == MOE_W_INT4_G32;
+  const bool rows_from_x = !int4 && d->T <= kGatherFromXTokens;
+  float* zero_router = rows_from_x ? zero_out : nullptr;
+  float* zero_gather = rows_from_x ? nullptr : zero_out;
   record(ev, 0, s);
+  if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s, zero_router)) != MOE_OK)
+    return st;
+  record(ev, 1, s);
   if (d->T <= kSmallT) {
-    // decode sizes: router, then one CTA for the whole permutation
-    if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
-    record(ev, 1, s);
+    // decode sizes: one CTA for the whole permutation
     if (launch_route_small(nullptr, d->T, d->E, d->top_k, pick_bn(d->T), idx, wts,
                            w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of), roww,
                            table, s) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T,
-                           d->fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
-                           zero_out ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
+    if (!rows_from_x &&
+        launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T, int4,
+                           static_cast<uint16_t*>(x_perm), zero_gather,
+                           zero_gather ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
-    if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s)) != MOE_OK) return st;
-    record(ev, 1, s);
     if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather,
-                          w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, zero_out)) != MOE_OK)
+                          w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, zero_gather,
+                          !rows_from_x)) != MOE_OK)
       return st;
   }
+  const void* rows_src = rows_from_x ? x : x_perm;
+  const int32_t* xrows = rows_from_x ? gather : nullptr;
   if (!det)
-    return run_experts(*d, x_perm, table, experts, shared, kEpiScatterAdd, gather, roww, out, w, s,
-                       ev);
+    return run_experts(*d, rows_src, table, experts, shared, kEpiScatterAdd, gather, roww, out, w,
+                       s, ev, xrows);
   // deterministic: unweighted rows, then the fixed-order combination
   float* y_perm = w.at<float>(L.y_perm);
-  if ((st = run_experts(*d, x_perm, table, experts, shared, kEpiStoreRows, nullptr, nullptr, y_perm,
-                        w, s, ev)) != MOE_OK)
+  if ((st = run_experts(*d, rows_src, table, experts, shared, kEpiStoreRows, nullptr, nullptr,
+                        y_perm, w, s, ev, xrows)) != MOE_OK)
     return st;
   const cudaError_t e = launch_combine(y_perm, w.at<int32_t>(L.row_of), wts, d->T, d->H,
                                        d->top_k, accumulate, out, s);

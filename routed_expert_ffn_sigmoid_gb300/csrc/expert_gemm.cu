@@ -71,6 +71,7 @@ struct DownCfg {
 
 struct GateUpArgs {
   const int32_t* table;
+  const int32_t* xrows;  // non-null: token rows gathered from x by xrows[r] (tm_x over x)
   int K, I, E, a_rows, total_rows;
   int ksplit;            // units per tile along K (1: no split)
   float* partial;        // ksplit > 1: fp32 partial G/U per unit
@@ -204,36 +205,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = a.K / kBK;
 
   if (warp == 0) {
-    if (lane == 0) {
+    // Producer warp.  Lane 0 waits for a free stage, arms it and loads the
+    // weight tiles; the token rows come either as 16-row boxes of x_perm
+    // (lane 0) or, with a.xrows, straight from x: lane L gathers rows
+    // 4L .. 4L+3 of the tile (tile::gather4), so no permuted copy of x exists.
+    // Only the tile's own rows are gathered (rounded up to 4); the rest of
+    // the 16-row MMA block keeps whatever an earlier stage left there, which
+    // reaches only output columns the epilogue never reads.
+    const bool gat = a.xrows != nullptr;
+    if (gat || lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
+      // A unit's table entry and gathered row indices are loaded one unit
+      // ahead: between two units the producer never waits on a global load,
+      // so the weight stream keeps its copies in flight.
+      TileEntry te_next{};
+      int tok_next[4] = {0, 0, 0, 0};
+      auto fetch_unit = [&](int uu) {
+        te_next = entry_at(a.table, 0, BN, (uu / a.ksplit) / mblocks);
+        if (gat && lane < (te_next.nrows + 3) / 4) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tok_next[j] = a.xrows[te_next.row0 + min(4 * lane + j, te_next.nrows - 1)];
+        }
+      };
+      if (blockIdx.x < units) fetch_unit(blockIdx.x);
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const int tile = u / a.ksplit, sp = u % a.ksplit;
         const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
-        const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+        const TileEntry te = te_next;
+        // gathered rows of this lane (rows past the group repeat its last row)
+        const int tok[4] = {tok_next[0], tok_next[1], tok_next[2], tok_next[3]};
+        if (u + static_cast<int>(gridDim.x) < units) fetch_unit(u + gridDim.x);
         const int mb = tile % mblocks;
         const bool sh = te.group == a.E;
         const CUtensorMap* mg = sh ? &tm_sgate : &tm_gate;
         const CUtensorMap* mu = sh ? &tm_sup : &tm_up;
         const int ge = sh ? 0 : te.group;
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
-        const uint32_t bytes = 2u * a.a_rows * kRowBytes + nchunks * kChunkBytes;
+        const int ngather = (te.nrows + 3) / 4;  // gather4 loads of the tile (gathered rows)
+        const uint32_t bytes = 2u * a.a_rows * kRowBytes +
+                               (gat ? ngather * 4 * kRowBytes : nchunks * kChunkBytes);
+        const bool issuer = gat && lane < ngather;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab)) {
+          uint8_t* st = sm.tiles + stage * Cfg::kStageBytes;
+          bool go = true;
+          if (lane == 0) {
+            go = mbar_wait(&sm.empty[stage], phase ^ 1u, ab);
+            if (go) {
+              mbar_arrive_expect_tx(&sm.full[stage], bytes);
+              armed |= 1u << stage;
+              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+              tma_load_3d(st, mg, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
+              tma_load_3d(st + kATileBytes, mu, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
+              if (!gat)
+                for (int c = 0; c < nchunks; ++c)
+                  tma_load_2d(st + 2 * kATileBytes + c * kChunkBytes, &tm_x, &sm.full[stage],
+                              kb * kBK, te.row0 + c * kChunkRows, pol_x);
+            }
+          }
+          if (gat) go = __shfl_sync(0xffffffffu, go, 0);
+          if (!go) {
             ok = false;
             break;
           }
-          uint8_t* st = sm.tiles + stage * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&sm.full[stage], bytes);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(st, mg, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
-          tma_load_3d(st + kATileBytes, mu, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
-          for (int c = 0; c < nchunks; ++c)
-            tma_load_2d(st + 2 * kATileBytes + c * kChunkBytes, &tm_x, &sm.full[stage], kb * kBK,
-                        te.row0 + c * kChunkRows, pol_x);
+          if (issuer)
+            tma_gather4_2d(st + 2 * kATileBytes + lane * 4 * kRowBytes, &tm_x, &sm.full[stage],
+                           kb * kBK, tok[0], tok[1], tok[2], tok[3], pol_x);
           if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -241,8 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // every copy issued has landed before the CTA may exit
-      for (int s = 0; s < Cfg::kStages; ++s)
-        if ((armed >> s) & 1u) mbar_wait_drain(&sm.full[s], (armed_par >> s) & 1u);
+      if (lane == 0)
+        for (int s = 0; s < Cfg::kStages; ++s)
+          if ((armed >> s) & 1u) mbar_wait_drain(&sm.full[s], (armed_par >> s) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -637,7 +678,7 @@ cudaError_t gateup_dispatch(const GateUpLaunch& L, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  GateUpArgs a{L.table, L.K, L.I, L.E, L.a_rows, L.total_rows, L.ksplit > 0 ? L.ksplit : 1,
+  GateUpArgs a{L.table, L.xrows, L.K, L.I, L.E, L.a_rows, L.total_rows, L.ksplit > 0 ? L.ksplit : 1,
                L.partial, L.counters, L.h0, L.h1, L.status, L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);

@@ -29,17 +29,20 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_route
                                       float* z, int T, int H, int E, cudaStream_t s);
 
 // Per token: top_k of z (ties to the lower index), sigmoid, renormalise.
+// The router kernels also clear zero_n floats of zero_out (the layer output,
+// when the down epilogue adds into it) with their whole grid.
 // Decode-size router: partial logits per reduction slice of kRouterSliceK
 // elements, part [slices][T][E] fp32, then per token the slice sum in slice
 // order + bias and the top-k (z [T][E] also written when z != nullptr).
 constexpr int kRouterSliceK = 256;
 inline int router_slices(int H) { return (H + kRouterSliceK - 1) / kRouterSliceK; }
 cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, float* part,
-                                  int T, int H, int E, cudaStream_t s);
+                                  int T, int H, int E, float* zero_out, size_t zero_n,
+                                  cudaStream_t s);
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
                                       int k, int32_t* idx, float* w, float* z, cudaStream_t s);
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
-                        cudaStream_t s);
+                        cudaStream_t s, float* zero_out = nullptr, size_t zero_n = 0);
 
 // ---------------------------------------------------------------- permute
 
@@ -84,6 +87,8 @@ cudaError_t launch_combine(const float* y_perm, const int32_t* row_of, const flo
 struct GateUpLaunch {
   CUtensorMap tm_gate, tm_up, tm_sgate, tm_sup, tm_x;
   const int32_t* table;
+  const int32_t* xrows;  // null: tm_x maps x_perm (16-row boxes); else tm_x maps x
+                         // (1-row boxes) and row r of the tile is x[xrows[r]]
   int BN;            // token tile (16, 32, 64, 128, 256)
   int K;             // H
   int I;             // intermediate size (features)

@@ -127,6 +127,20 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Four rows r0..r3 (any order, any rows) of a 2-D map whose box is one row
+// high, written to dst as four consecutive box rows (same swizzle as a box
+// load of four rows there): TMA's tile::gather4 load.
+__device__ __forceinline__ void tma_gather4_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                               int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
   asm volatile(

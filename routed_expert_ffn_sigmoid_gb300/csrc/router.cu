@@ -147,10 +147,19 @@ __device__ __forceinline__ void partial_dot(const float* xs, const float* wsm, i
   }
 }
 
+// Clears n4 float4s of `out` with every thread of the grid (the layer's
+// output when the down epilogue adds into it; null: nothing to clear).
+__device__ __forceinline__ void clear_grid(float4* out, size_t n4) {
+  if (!out) return;
+  const size_t nthr = static_cast<size_t>(gridDim.x) * gridDim.y * blockDim.x;
+  const size_t i0 = (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+  for (size_t i = i0; i < n4; i += nthr) out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // grid (ceil(E / 32), ceil(H / kRouterSliceK)), kPartThreads threads.
 __global__ void __launch_bounds__(kPartThreads) router_partial_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, int T, int H, int E,
-    float* __restrict__ part) {
+    float* __restrict__ part, float4* __restrict__ zero_out, size_t zero_n4) {
   extern __shared__ float4 smem_f4[];
   float* xs = reinterpret_cast<float*>(smem_f4);  // [kPartTok][kPartRow]
   float* wsm = xs + kPartTok * kPartRow;          // [kPartExperts][kPartRow]
@@ -161,6 +170,7 @@ __global__ void __launch_bounds__(kPartThreads) router_partial_kernel(
   constexpr int kChunksPerRow = kRouterSliceK / 8;
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  clear_grid(zero_out, zero_n4);
   // router rows of the block (zero past E and past H)
   uint4 wv[kPartWLoads];
 #pragma unroll
@@ -264,9 +274,12 @@ __global__ void __launch_bounds__(kMaxE) router_reduce_topk_kernel(
 // One warp per token: top-k, sigmoid, renormalisation.
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ z, int T, int E,
                                                    int k, int32_t* __restrict__ idx,
-                                                   float* __restrict__ w) {
+                                                   float* __restrict__ w,
+                                                   float4* __restrict__ zero_out,
+                                                   size_t zero_n4) {
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  clear_grid(zero_out, zero_n4);
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t < T) {
@@ -296,7 +309,8 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_route
 }
 
 cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, float* part,
-                                  int T, int H, int E, cudaStream_t s) {
+                                  int T, int H, int E, float* zero_out, size_t zero_n,
+                                  cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   cudaError_t err = cudaFuncSetAttribute(router_partial_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -304,7 +318,7 @@ cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, 
   if (err != cudaSuccess) return err;
   const dim3 grid((E + kPartExperts - 1) / kPartExperts, router_slices(H));
   return launch_pdl(router_partial_kernel, grid, dim3(kPartThreads), kPartSmem, s, x, w_router,
-                    T, H, E, part);
+                    T, H, E, part, reinterpret_cast<float4*>(zero_out), zero_n / 4);
 }
 
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
@@ -316,9 +330,10 @@ cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, 
 }
 
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
-                        cudaStream_t s) {
+                        cudaStream_t s, float* zero_out, size_t zero_n) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, z, T, E, k, idx, w);
+  return launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, z, T, E, k, idx, w,
+                    reinterpret_cast<float4*>(zero_out), zero_n / 4);
 }
 
 }  // namespace moe
