@@ -448,14 +448,16 @@ def run_ours(args, wl, rank, world, local):
 
 def layer_launches(T, deterministic, fmt="bf16"):
     """Kernels one moe_ffn_forward launches.  T <= 128: router partial logits,
-    slice sum + top-k, one-CTA permutation, gate/up, down.  Larger T: logits
-    (partial sums below 256 tokens, tensor cores from 256), top-k, count,
-    scan, scatter, gate/up, down.  The bf16 gate/up GEMM gathers the token rows
-    from x itself up to 8 tokens; above, and always for Int4, one more kernel
-    writes x_perm.  Deterministic mode adds the fixed-order combination."""
+    slice sum + top-k, the one-CTA permutation (for T <= 16 run by the top-k
+    kernel's last CTA instead), gate/up, down.
+    Larger T: logits (partial sums below 256 tokens, tensor cores from 256),
+    top-k, count, scan, scatter, gate/up, down.  The bf16 gate/up GEMM gathers
+    the token rows from x itself up to 8 tokens; above, and always for Int4,
+    one more kernel writes x_perm.  Deterministic mode adds the fixed-order
+    combination."""
     gathers_itself = fmt == "bf16" and T <= 8
-    return ((5 if T <= 128 else 7) + (0 if gathers_itself else 1)
-            + (1 if deterministic else 0))
+    base = 4 if T <= 16 else (5 if T <= 128 else 7)
+    return base + (0 if gathers_itself else 1) + (1 if deterministic else 0)
 
 
 def run_dense(args, rank, world, local):

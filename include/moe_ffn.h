@@ -187,8 +187,10 @@ moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_route
 /*
  * Stage boundaries of moe_ffn_forward_timed: ev[i] is recorded on `stream`
  * before stage i, ev[MOE_STAGE_COUNT] after the last one.  Stages:
- *   0 router logits + top-k      1 permutation (count, scan, scatter, gather;
- *                                  one kernel + gather for T <= 128)
+ *   0 router logits + top-k (for T <= 16 also the permutation, run by the
+ *     top-k kernel's last CTA)   1 permutation (one CTA for T <= 128; count,
+ *     scan, scatter above) and the gather of x_perm (bf16 weights and T <= 8:
+ *     none; the gate/up GEMM gathers its token rows from x itself)
  *   2 grouped gate/up + SwiGLU   3 grouped down + weighted scatter-add
  * Each ev[i] is a cudaEvent_t created by the caller (NULL entries are skipped).
  * When `stream` is being captured into a CUDA graph the records are captured

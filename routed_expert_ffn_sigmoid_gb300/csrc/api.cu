@@ -17,8 +17,10 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;        // status word + reserved
+constexpr size_t kRouteDoneOffset = 64;     // header: CTAs of the top-k kernel done (zero between calls)
 constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many tokens
 constexpr int kGatherFromXTokens = 8;       // bf16 gate/up gathers its token rows from x up to this
+constexpr int kFusedPermTokens = 16;        // the top-k kernel's last CTA permutes up to this
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -239,6 +241,7 @@ struct Ws {
   char* base;
   Layout L;
   int* status() const { return reinterpret_cast<int*>(base); }
+  int* route_done() const { return reinterpret_cast<int*>(base + kRouteDoneOffset); }
   template <typename T>
   T* at(size_t off) const {
     return reinterpret_cast<T*>(base + off);
@@ -259,10 +262,11 @@ moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes, Ws* out) {
 // from the tensor cores (bias in the epilogue) and a warp per token selects;
 // below, partial logits per reduction slice spread the router matrix over
 // all SMs and a warp per token adds the slices, the bias and selects.
-// With zero_out, the router's kernels also clear out [T][H].
+// With zero_out, the router's kernels also clear out [T][H]; with perm
+// (T <= kSmallT) the top-k kernel's last CTA also runs the permutation.
 moe_status run_router(const moe_dims& d, const void* x, const void* w_router, const float* b,
                       int32_t* idx, float* w, const Ws& ws, cudaStream_t s,
-                      float* zero_out = nullptr) {
+                      float* zero_out = nullptr, const SmallPermOut* perm = nullptr) {
   float* z = ws.at<float>(ws.L.z);
   const size_t zero_n = zero_out ? static_cast<size_t>(d.T) * d.H : 0;
   if (d.T < kRouterTcMinTokens) {
@@ -271,7 +275,7 @@ moe_status run_router(const moe_dims& d, const void* x, const void* w_router, co
                                zero_out, zero_n, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     return from_cuda(
-        launch_router_reduce_topk(z, b, d.T, d.H, d.E, d.top_k, idx, w, nullptr, s));
+        launch_router_reduce_topk(z, b, d.T, d.H, d.E, d.top_k, idx, w, nullptr, perm, s));
   }
   cudaError_t e;
   {
@@ -580,15 +584,19 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   const bool rows_from_x = !int4 && d->T <= kGatherFromXTokens;
   float* zero_router = rows_from_x ? zero_out : nullptr;
   float* zero_gather = rows_from_x ? nullptr : zero_out;
+  // decode sizes: one CTA permutes; up to kFusedPermTokens tokens it is the
+  // top-k kernel's last CTA (one launch fewer), above a launch of its own
+  // with more threads (measured faster at 64 tokens)
+  const SmallPermOut perm{w.route_done(), pick_bn(d->T), w.at<int32_t>(L.offsets), gather,
+                          w.at<int32_t>(L.row_of), roww, table};
+  const bool small = d->T <= kSmallT, fused = d->T <= kFusedPermTokens;
   record(ev, 0, s);
-  if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s, zero_router)) != MOE_OK)
+  if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s, zero_router,
+                       fused ? &perm : nullptr)) != MOE_OK)
     return st;
   record(ev, 1, s);
-  if (d->T <= kSmallT) {
-    // decode sizes: one CTA for the whole permutation
-    if (launch_route_small(nullptr, d->T, d->E, d->top_k, pick_bn(d->T), idx, wts,
-                           w.at<int32_t>(L.offsets), gather, w.at<int32_t>(L.row_of), roww,
-                           table, s) != cudaSuccess)
+  if (small) {
+    if (!fused && launch_small_permutation(idx, wts, d->T, d->E, d->top_k, perm, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rows_from_x &&
         launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T, int4,

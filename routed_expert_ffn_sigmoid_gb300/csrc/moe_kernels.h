@@ -39,8 +39,24 @@ inline int router_slices(int H) { return (H + kRouterSliceK - 1) / kRouterSliceK
 cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, float* part,
                                   int T, int H, int E, float* zero_out, size_t zero_n,
                                   cudaStream_t s);
+// Outputs of the decode-size permutation (T <= kSmallT), which the last CTA
+// of the top-k kernel runs once every token's selection is written; `done`
+// is a counter that is zero before the launch and zero again after it.
+struct SmallPermOut {
+  int* done;
+  int BN;
+  int32_t* offsets;
+  int32_t* gather;
+  int32_t* row_of;
+  float* roww;
+  int32_t* table;
+};
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
-                                      int k, int32_t* idx, float* w, float* z, cudaStream_t s);
+                                      int k, int32_t* idx, float* w, float* z,
+                                      const SmallPermOut* perm, cudaStream_t s);
+// The same permutation as a one-CTA launch of its own (`done` unused).
+cudaError_t launch_small_permutation(const int32_t* idx, const float* w, int T, int E, int k,
+                                     const SmallPermOut& p, cudaStream_t s);
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s, float* zero_out = nullptr, size_t zero_n = 0);
 
@@ -62,12 +78,6 @@ cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
                                bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
                                cudaStream_t s);
-// T <= kSmallT: top-k (from the logits z, or z == nullptr: read from idx / w),
-// histogram, offsets, stable ranks, gather / row_of / row weights and the
-// tile table in one CTA.
-cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
-                               float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
-                               float* roww, int32_t* table, cudaStream_t s);
 // Dense FFN: rows 0..T-1 are one group (group 0): gather[r] = r, roww[r] = 1
 // and a tile table of ceil(T / BN) entries.
 cudaError_t launch_dense_rows(int T, int BN, int32_t* gather, float* roww, int32_t* table,

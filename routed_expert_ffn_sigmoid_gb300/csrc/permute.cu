@@ -230,91 +230,28 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
   if (threadIdx.x == 0) table[0] = min(n_entries, capacity);
 }
 
-// Decode-size routing in one CTA (T <= kSmallT tokens): per-token top-k of
-// the logits z (or, with z null, the selection already in idx / w), expert
-// histogram, exclusive offsets (shared expert appended as group E),
-// stable ranks from per-expert token bitmaps, gather / row_of / row weights
-// and the tile table -- the work of the top-k, count, scan and scatter
-// kernels without three launches in between.
-__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
-    const float* __restrict__ z, int T, int E, int k, int BN, int32_t* __restrict__ idx_out,
-    float* __restrict__ w_out, int32_t* __restrict__ offsets, int32_t* __restrict__ gather,
-    int32_t* __restrict__ row_of, float* __restrict__ roww, int32_t* __restrict__ table) {
-  __shared__ int s_idx[kSmallT * kMaxTopK];
-  __shared__ float s_w[kSmallT * kMaxTopK];
-  __shared__ int cnt[kMaxE + 2];
-  __shared__ int ntile[kMaxE + 1];
-  __shared__ uint32_t bits[kMaxE][kSmallT / 32];
-  __shared__ int total_rows, n_entries;
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) cnt[g] = 0;
-  for (int i = threadIdx.x; i < E * (kSmallT / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
+}  // namespace
+
+namespace {
+
+// The decode-size permutation as a launch of its own (one CTA).
+__global__ void __launch_bounds__(kSmallThreads) small_permutation_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int E, int k, int BN,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ gather, int32_t* __restrict__ row_of,
+    float* __restrict__ roww, int32_t* __restrict__ table) {
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (z) {
-    for (int t = warp; t < T; t += kSmallThreads / 32) {
-      int e;
-      float wv;
-      warp_topk(z + static_cast<size_t>(t) * E, E, k, &e, &wv);
-      if (lane < k) {
-        s_idx[t * k + lane] = e;
-        s_w[t * k + lane] = wv;
-        idx_out[t * k + lane] = e;
-        w_out[t * k + lane] = wv;
-      }
-    }
-  } else {  // the selection is already in idx / w
-    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
-      s_idx[i] = idx_out[i];
-      s_w[i] = w_out[i];
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
-    const int t = i / k, e = s_idx[i];
-    atomicAdd(&cnt[e], 1);
-    atomicOr(&bits[e][t >> 5], 1u << (t & 31));
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) cnt[E] = T;
-  __syncthreads();
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (cnt[g] + BN - 1) / BN;
-  warp0_exclusive_scan(cnt, E + 1, &total_rows);  // cnt becomes the offsets
-  __syncthreads();
-  if (threadIdx.x == 0) cnt[E + 1] = total_rows;
-  __syncthreads();
-  for (int g = threadIdx.x; g <= E + 1; g += blockDim.x) offsets[g] = cnt[g];
-  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
-    const int t = i / k, e = s_idx[i];
-    int rank = __popc(bits[e][t >> 5] & ((1u << (t & 31)) - 1u));
-    for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bits[e][wd]);
-    const int r = cnt[e] + rank;
-    gather[r] = t;
-    row_of[i] = r;
-    roww[r] = s_w[i];
-  }
-  for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    gather[k * T + t] = t;
-    roww[k * T + t] = 1.0f;
-  }
-  warp0_exclusive_scan(ntile, E + 1, &n_entries);
-  __syncthreads();
-  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
-    const int o = cnt[g], c = cnt[g + 1] - o;
-    for (int i = 0, r = 0; r < c; ++i, r += BN) {
-      TileEntry te;
-      te.group = g;
-      te.row0 = o + r;
-      te.nrows = min(BN, c - r);
-      te.pad = 0;
-      ent[ntile[g] + i] = te;
-    }
-  }
-  if (threadIdx.x == 0) table[0] = n_entries;
+  small_permutation(idx, w, T, E, k, BN, offsets, gather, row_of, roww, table);
 }
 
 }  // namespace
+
+cudaError_t launch_small_permutation(const int32_t* idx, const float* w, int T, int E, int k,
+                                     const SmallPermOut& p, cudaStream_t s) {
+  if (T == 0 || T > kSmallT) return cudaErrorInvalidValue;
+  return launch_pdl(small_permutation_kernel, dim3(1), dim3(kSmallThreads), 0, s, idx, w, T, E,
+                    k, p.BN, p.offsets, p.gather, p.row_of, p.roww, p.table);
+}
 
 cudaError_t launch_perm_count(const int32_t* idx, int T, int E, int k, int32_t* blockcnt,
                               cudaStream_t s) {
@@ -357,13 +294,6 @@ cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, i
                     capacity, table, BN);
 }
 
-cudaError_t launch_route_small(const float* z, int T, int E, int k, int BN, int32_t* idx,
-                               float* w, int32_t* offsets, int32_t* gather, int32_t* row_of,
-                               float* roww, int32_t* table, cudaStream_t s) {
-  if (T == 0 || T > kSmallT) return cudaErrorInvalidValue;
-  return launch_pdl(route_small_kernel, dim3(1), dim3(kSmallThreads), 0, s, z, T, E, k, BN, idx,
-                    w, offsets, gather, row_of, roww, table);
-}
 
 namespace {
 

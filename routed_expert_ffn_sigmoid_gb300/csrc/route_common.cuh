@@ -100,6 +100,76 @@ __device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) 
   if (lane == 0) *total = carry;
 }
 
+// Decode-size permutation by one CTA (T <= kSmallT tokens, any block size
+// that is a multiple of 32): from the top-k selection idx / w [T][k] in
+// global memory, the expert histogram, exclusive offsets (the shared expert
+// appended as group E), stable ranks from per-expert token bitmaps,
+// gather / row_of / row weights and the tile table -- the work of the count,
+// scan and scatter kernels with no launch in between.  The selection was
+// written by other CTAs of the calling grid: it is read past L1.
+__device__ __forceinline__ void small_permutation(const int32_t* idx, const float* w, int T, int E,
+                                                  int k, int BN, int32_t* __restrict__ offsets,
+                                                  int32_t* __restrict__ gather,
+                                                  int32_t* __restrict__ row_of,
+                                                  float* __restrict__ roww,
+                                                  int32_t* __restrict__ table) {
+  __shared__ int s_idx[kSmallT * kMaxTopK];
+  __shared__ float s_w[kSmallT * kMaxTopK];
+  __shared__ int cnt[kMaxE + 2];
+  __shared__ int ntile[kMaxE + 1];
+  __shared__ uint32_t bits[kMaxE][kSmallT / 32];
+  __shared__ int total_rows, n_entries;
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) cnt[g] = 0;
+  for (int i = threadIdx.x; i < E * (kSmallT / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    s_idx[i] = __ldcg(idx + i);
+    s_w[i] = __ldcg(w + i);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k, e = s_idx[i];
+    atomicAdd(&cnt[e], 1);
+    atomicOr(&bits[e][t >> 5], 1u << (t & 31));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) cnt[E] = T;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (cnt[g] + BN - 1) / BN;
+  warp0_exclusive_scan(cnt, E + 1, &total_rows);  // cnt becomes the offsets
+  __syncthreads();
+  if (threadIdx.x == 0) cnt[E + 1] = total_rows;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E + 1; g += blockDim.x) offsets[g] = cnt[g];
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k, e = s_idx[i];
+    int rank = __popc(bits[e][t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bits[e][wd]);
+    const int r = cnt[e] + rank;
+    gather[r] = t;
+    row_of[i] = r;
+    roww[r] = s_w[i];
+  }
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    gather[k * T + t] = t;
+    roww[k * T + t] = 1.0f;
+  }
+  warp0_exclusive_scan(ntile, E + 1, &n_entries);
+  __syncthreads();
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int o = cnt[g], c = cnt[g + 1] - o;
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      TileEntry te;
+      te.group = g;
+      te.row0 = o + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = n_entries;
+}
+
 // Launch helper: programmatic stream serialization lets a kernel begin while
 // its predecessor drains; every kernel launched this way calls pdl_wait()
 // before it touches data a predecessor produced.  The routing kernels call

@@ -232,7 +232,8 @@ constexpr int kReduceBatch = 16;  // slice loads in flight per thread
 
 __global__ void __launch_bounds__(kMaxE) router_reduce_topk_kernel(
     const float* __restrict__ part, const float* __restrict__ b, int T, int E, int slices, int k,
-    int32_t* __restrict__ idx, float* __restrict__ w, float* __restrict__ z_out) {
+    int32_t* __restrict__ idx, float* __restrict__ w, float* __restrict__ z_out,
+    const SmallPermOut perm) {
   __shared__ uint32_t keys_s[kMaxE];
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
@@ -267,6 +268,20 @@ __global__ void __launch_bounds__(kMaxE) router_reduce_topk_kernel(
     if (lane < k) {
       idx[static_cast<size_t>(t) * k + lane] = e;
       w[static_cast<size_t>(t) * k + lane] = wv;
+    }
+  }
+  if (perm.done) {
+    // the last CTA to finish runs the permutation over every token's selection
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(perm.done, 1) == static_cast<int>(gridDim.x) - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      small_permutation(idx, w, T, E, k, perm.BN, perm.offsets, perm.gather, perm.row_of,
+                        perm.roww, perm.table);
+      if (threadIdx.x == 0) *perm.done = 0;
     }
   }
 }
@@ -322,11 +337,14 @@ cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, 
 }
 
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
-                                      int k, int32_t* idx, float* w, float* z, cudaStream_t s) {
+                                      int k, int32_t* idx, float* w, float* z,
+                                      const SmallPermOut* perm, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (perm && T > kSmallT) return cudaErrorInvalidValue;
+  const SmallPermOut none{};
   const int threads = ((E + 31) / 32) * 32;  // E <= kMaxE
   return launch_pdl(router_reduce_topk_kernel, dim3(T), dim3(threads), 0, s, part, b, T, E,
-                    router_slices(H), k, idx, w, z);
+                    router_slices(H), k, idx, w, z, perm ? *perm : none);
 }
 
 cudaError_t launch_topk(const float* z, int T, int E, int k, int32_t* idx, float* w,
