@@ -42,6 +42,7 @@ struct TmCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
   static_assert(kAccStages * kAccCols <= 512, "TMEM");
+  static_assert(NBM * FN <= 256, "one MMA spans every weight tile of a stage");
   static_assert(kStageBytes % 1024 == 0, "alignment");
 };
 
@@ -163,7 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kBM, FN, true);
+      // gate/up: the gate and up tiles lie back to back in shared memory, so
+      // one N = 256 MMA covers both (columns 0..127 gate, 128..255 up) and
+      // reads each token tile once per K step instead of twice
+      const uint32_t idesc = idesc_f16(kBM, NBM * FN, true);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -181,13 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da0 = sw128_kmajor_desc(st);
           const uint64_t da1 = sw128_kmajor_desc(st + kATileBytes);
           const uint64_t db0 = sw128_kmajor_desc(st + NA * kATileBytes);
-          const uint64_t db1 = sw128_kmajor_desc(st + NA * kATileBytes + Cfg::kBTileBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accum = (kb | k) != 0;
             umma_f16(d0, da0 + 2 * k, db0 + 2 * k, idesc, accum);
             if (NA == 2) umma_f16(d0, da1 + 2 * k, db0 + 2 * k, idesc, 1u);
-            if (NBM == 2) umma_f16(d0 + FN, da0 + 2 * k, db1 + 2 * k, idesc, accum);
           }
           umma_commit(&empty[stage]);
           if (++stage == Cfg::kStages) {
