@@ -1,0 +1,99 @@
+"""GPU edge cases of the routing and the layer: exact ties at the top-k
+boundary, every logit tied, and the largest expert count and top-k the
+library accepts, each against the oracle.
+
+Ties: the pages ask for a deterministic top-k, which the oracle reads as
+"equal scores go to the lower expert index" ("feat(glm53): add
+device-resident HIP backend for MI350P", Key changes).  Identical router
+rows and biases give logits that are equal bit for bit on either side, so
+the selection must be exactly the lowest tied indices."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from moe_inputs import make_inputs, rel_max_err
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import routed_expert_ffn_sigmoid_gb300 as moe  # noqa: E402
+from gpu_helpers import TOL, dev_u16, upload_matrices, weights_struct  # noqa: E402
+
+TINY = synthetic.WORKLOADS["tiny"]  # H = 256, E = 288, I = 64
+TIED = [3, 17, 40, 41, 100, 200, 250, 260, 270, 287]  # ten experts, one row
+
+
+def _route(wl, x, w_router, b_router, T):
+    dims = moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, wl.top_k), dtype=torch.float32, device="cuda")
+    moe.moe_router_topk(dims, dev_u16(x), dev_u16(w_router), torch.from_numpy(b_router).cuda(),
+                        idx, w, ws)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+def _forward(wl, x, w_router, b_router, ex, sh, T):
+    dims = moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    out = torch.full((T, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_ffn_forward(dims, dev_u16(x), dev_u16(w_router), torch.from_numpy(b_router).cuda(),
+                        weights_struct(upload_matrices(ex)), weights_struct(upload_matrices(sh)),
+                        out, ws)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    return out.cpu().numpy()
+
+
+# T = 8: CUDA-core partial logits; T = 300: the tensor-core router
+@pytest.mark.parametrize("T", [8, 300])
+def test_exact_ties_go_to_the_lower_expert(T):
+    wl = replace(TINY, T=T)
+    w_router, b_router = synthetic.gen_router(wl)
+    w_router = w_router.copy()
+    b_router = b_router.copy()
+    w_router[TIED] = w_router[TIED[0]]
+    b_router[TIED] = 8.0  # far above every other logit: the ten tie for the top
+    x = synthetic.gen_x(wl, T=T)
+    idx, w = _route(wl, x, w_router, b_router, T)
+    want = np.array(TIED[:wl.top_k], np.int32)
+    assert np.array_equal(np.sort(idx, axis=1), np.broadcast_to(want, idx.shape))
+    assert np.all(w == np.float32(0.125))  # equal scores renormalise to 1/8 exactly
+    r_idx, r_w = oracle.topk(oracle.router_logits(x, w_router, b_router), wl.top_k)[:2]
+    assert np.array_equal(np.sort(r_idx, axis=1), np.sort(idx, axis=1))
+    if T == 8:
+        inp = make_inputs(wl, T=T)
+        ref, _, _ = oracle.moe_forward(x, w_router, b_router, inp.experts, inp.shared, wl.fmt)
+        out = _forward(wl, x, w_router, b_router, inp.experts, inp.shared, T)
+        assert rel_max_err(out, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_all_logits_tied_selects_the_first_experts(T):
+    wl = replace(TINY, T=T)
+    w_router = np.zeros((wl.E, wl.H), np.uint16)  # bf16 +0
+    b_router = np.zeros(wl.E, np.float32)
+    x = synthetic.gen_x(wl, T=T)
+    idx, w = _route(wl, x, w_router, b_router, T)
+    assert np.array_equal(np.sort(idx, axis=1),
+                          np.broadcast_to(np.arange(wl.top_k, dtype=np.int32), idx.shape))
+    assert np.all(w == np.float32(0.125))
+
+
+def test_largest_expert_count_and_top_k():
+    """E = 512 experts and top_k = 16 (the library's limits), T = 40: every
+    slot, group and permutation array at its maximum width."""
+    wl = synthetic.Workload("edge_max", 40, 256, 512, 64, 64, 16, "bf16", 7, tokens=(40,))
+    inp = make_inputs(wl)
+    ref, r_idx, r_w = oracle.moe_forward(inp.x, inp.w_router, inp.b_router, inp.experts,
+                                         inp.shared, wl.fmt, top_k=wl.top_k)
+    idx, w = _route(wl, inp.x, inp.w_router, inp.b_router, wl.T)
+    assert np.array_equal(np.sort(idx, axis=1), np.sort(r_idx, axis=1))
+    out = _forward(wl, inp.x, inp.w_router, inp.b_router, inp.experts, inp.shared, wl.T)
+    assert rel_max_err(out, ref) <= TOL["bf16"]
