@@ -122,6 +122,32 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// 4 x 4 transpose across the four lanes 4j .. 4j+3 of a warp: lane 4j+r
+// holds row r, (x0, x1, x2, x3) = M[r][0..3], and ends with column r,
+// M[0..3][r].  Two exchange rounds (partner lane ^ 1, then ^ 2).
+__device__ __forceinline__ void transpose4_lanes(float& x0, float& x1, float& x2, float& x3,
+                                                 int lane) {
+  const bool o1 = lane & 1, o2 = lane & 2;
+  float s0 = __shfl_xor_sync(0xffffffffu, o1 ? x0 : x1, 1);
+  float s1 = __shfl_xor_sync(0xffffffffu, o1 ? x2 : x3, 1);
+  if (o1) {
+    x0 = s0;
+    x2 = s1;
+  } else {
+    x1 = s0;
+    x3 = s1;
+  }
+  s0 = __shfl_xor_sync(0xffffffffu, o2 ? x0 : x2, 2);
+  s1 = __shfl_xor_sync(0xffffffffu, o2 ? x1 : x3, 2);
+  if (o2) {
+    x0 = s0;
+    x1 = s1;
+  } else {
+    x2 = s0;
+    x3 = s1;
+  }
+}
+
 __device__ __forceinline__ __half bf16_bits_to_half(uint32_t bits16) {
   return __float2half_rn(__uint_as_float(bits16 << 16));
 }
@@ -413,7 +439,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x16(tq + c0, v0);
         if (NA == 2) tmem_ld_32x32b_x16(tq + BN + c0, v1);
         tmem_ld_wait();
-        if (f < a.N_out) {
+        if (NA == 1 && EPI == kEpiScatterAdd) {
+          // Lanes 4j .. 4j+3 hold four consecutive features; a 4 x 4 exchange
+          // leaves lane 4j+r with those four features of token column
+          // 4g + r, added with one 16-byte atomic instead of four scalar ones.
+          const int r4 = lane & 3;
+          float* const ob = a.out + (f & ~3);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float x0 = __uint_as_float(v0[4 * g]), x1 = __uint_as_float(v0[4 * g + 1]);
+            float x2 = __uint_as_float(v0[4 * g + 2]), x3 = __uint_as_float(v0[4 * g + 3]);
+            transpose4_lanes(x0, x1, x2, x3, lane);
+            const int c = c0 + 4 * g + r4;
+            const int rr = te.row0 + c;
+            if (c < te.nrows && rr < a.total_rows && f < a.N_out) {
+              const int t = a.gather[rr];
+              if (t >= 0 && t < a.out_rows) {
+                const float wr = a.roww[rr];
+                atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(t) * a.N_out),
+                          make_float4(wr * x0, wr * x1, wr * x2, wr * x3));
+              }
+            }
+          }
+        } else if (f < a.N_out) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = c0 + i;
@@ -423,10 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (NA == 2) {
                 const float hv = clamped_swiglu(d, __uint_as_float(v1[i]));
                 a.h[static_cast<size_t>(rr) * a.N_out + f_op] = __float2half_rn(hv);
-              } else if (EPI == kEpiScatterAdd) {
-                const int t = a.gather[rr];
-                if (t >= 0 && t < a.out_rows)
-                  atomicAdd(a.out + static_cast<size_t>(t) * a.N_out + f, a.roww[rr] * d);
               } else {
                 a.out[static_cast<size_t>(rr) * a.N_out + f] = d;
               }
