@@ -452,10 +452,10 @@ def layer_launches(T, deterministic, fmt="bf16"):
     kernel's last CTA instead), gate/up, down.
     Larger T: logits (partial sums below 256 tokens, tensor cores from 256),
     top-k, count, scan, scatter, gate/up, down.  The bf16 gate/up GEMM gathers
-    the token rows from x itself up to 8 tokens; above, and always for Int4,
-    one more kernel writes x_perm.  Deterministic mode adds the fixed-order
-    combination."""
-    gathers_itself = fmt == "bf16" and T <= 8
+    the token rows from x itself up to 8 tokens and from 512 tokens (its
+    token-major form); in between, and always for Int4, one more kernel writes
+    x_perm.  Deterministic mode adds the fixed-order combination."""
+    gathers_itself = fmt == "bf16" and (T <= 8 or T >= 512)
     base = 4 if T <= 16 else (5 if T <= 128 else 7)
     return base + (0 if gathers_itself else 1) + (1 if deterministic else 0)
 

@@ -21,6 +21,7 @@ constexpr size_t kRouteDoneOffset = 64;     // header: CTAs of the top-k kernel 
 constexpr int kRouterTcMinTokens = 256;     // tensor-core router from this many tokens
 constexpr int kGatherFromXTokens = 8;       // bf16 gate/up gathers its token rows from x up to this
 constexpr int kFusedPermTokens = 16;        // the top-k kernel's last CTA permutes up to this
+constexpr int kTmGatherMinTokens = 512;     // token-major gate/up copies its token rows from x from here
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -32,6 +33,9 @@ struct Layout {
 };
 
 int rows_of(const moe_dims& d) { return (d.top_k + 1) * d.T; }
+
+// Token-major grouped GEMMs (tokens as M) serve 128-token tiles.
+bool token_major(const moe_dims& d);
 
 int pick_bn(int T) {
   if (T <= 16) return 16;
@@ -72,6 +76,10 @@ int split_for(long tiles, int KB, int nsm) {
     if (rem == 0 || 2 * rem >= nsm || full >= 4) return S;
   }
   return 1;
+}
+
+bool token_major(const moe_dims& d) {
+  return d.fmt == MOE_W_BF16 && pick_bn(d.T) == 128 && d.I % 128 == 0 && d.H % 256 == 0;
 }
 
 Layout layout_of(const moe_dims& d) {
@@ -349,7 +357,7 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
                        const moe_weights* ex, const moe_weights* sh, int epilogue,
                        const int32_t* gather, const float* roww, float* out, const Ws& ws,
                        cudaStream_t s, const moe_stage_events* ev = nullptr,
-                       const int32_t* xrows = nullptr) {
+                       const int32_t* xrows = nullptr, float* zero_out = nullptr) {
   const int rows = rows_of(d);
   const int BN = pick_bn(d.T);
   const int nsm = sm_count();
@@ -415,11 +423,11 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     return from_cuda(e);
   }
 
-  if (BN == 128 && d.I % 128 == 0 && d.H % 256 == 0) {
+  if (token_major(d)) {
     // token-major kernels: tiles of up to 128 rows of one group
     TmLaunch G{};
-    if (xrows) return MOE_ERR_UNSUPPORTED;  // token-major tiles read x_perm
-    if (!encode_kmajor(&G.tm_a[0], x_perm, true, d.H, rows, 1, 128) ||
+    // with xrows the producer warp copies the token rows from x itself
+    if (!encode_kmajor(&G.tm_a[0], x_perm, true, d.H, xrows ? d.T : rows, 1, 128) ||
         !encode_weights(&G.tm_b[0], ex->gate, true, d.H, d.I, d.E, 128) ||
         !encode_weights(&G.tm_b[1], ex->up, true, d.H, d.I, d.E, 128) ||
         !encode_weights(&G.tm_sb[0], sh->gate, true, d.H, d.I, 1, 128) ||
@@ -427,6 +435,11 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
       return MOE_ERR_CUDA;
     G.tm_a[1] = G.tm_a[0];
     G.table = table;
+    G.arows = xrows;
+    G.xsrc = x_perm;
+    G.xpitch = d.H;
+    G.zero_out = zero_out;
+    G.zero_n = zero_out ? static_cast<size_t>(d.T) * d.H : 0;
     G.gateup = true;
     G.K = d.H;
     G.N_out = d.I;
@@ -574,16 +587,22 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   // out is cleared (by the router kernels, or for Int4 by the gather that
   // converts x) only when the down epilogue adds into it
   float* zero_out = (det || accumulate) ? nullptr : out;
-  // bf16 weights, up to kGatherFromXTokens tokens: the gate/up GEMM gathers
-  // each token row straight from x (tile::gather4), so the permuted copy of x
-  // and its kernel drop out.  The gathers cost the copy engine about 3 % of
-  // the gate/up time on every stage, more than the copy kernel they replace
-  // once T grows (measured), so larger T reads a materialised x_perm; Int4
-  // always needs the fp16 copy in its operand order.
+  // bf16 weights: the gate/up GEMM gathers each token row straight from x,
+  // so the permuted copy of x and its kernel drop out -- up to
+  // kGatherFromXTokens tokens by TMA tile::gather4 (above that the gathers
+  // cost the copy engine more than the copy kernel, measured), and from
+  // kTmGatherMinTokens tokens in the token-major kernels by cp.async from a
+  // gather warp (measured: -3.1 % per step at 4096 tokens, -0.6 % at 512,
+  // +0.8 % at 128).  Int4 needs the fp16 copy in its operand order.
   const bool int4 = d->fmt == MOE_W_INT4_G32;
-  const bool rows_from_x = !int4 && d->T <= kGatherFromXTokens;
-  float* zero_router = rows_from_x ? zero_out : nullptr;
+  const bool tm = token_major(*d);
+  const bool rows_from_x =
+      !int4 && (d->T <= kGatherFromXTokens || (tm && d->T >= kTmGatherMinTokens));
+  // who clears out: the gather kernel when it runs, else the token-major
+  // gate/up kernel's idle epilogue warps, else the router's kernels
   float* zero_gather = rows_from_x ? nullptr : zero_out;
+  float* zero_gemm = rows_from_x && tm ? zero_out : nullptr;
+  float* zero_router = rows_from_x && !tm ? zero_out : nullptr;
   // decode sizes: one CTA permutes; up to kFusedPermTokens tokens it is the
   // top-k kernel's last CTA (one launch fewer), above a launch of its own
   // with more threads (measured faster at 64 tokens)
@@ -613,11 +632,11 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   const int32_t* xrows = rows_from_x ? gather : nullptr;
   if (!det)
     return run_experts(*d, rows_src, table, experts, shared, kEpiScatterAdd, gather, roww, out, w,
-                       s, ev, xrows);
+                       s, ev, xrows, zero_gemm);
   // deterministic: unweighted rows, then the fixed-order combination
   float* y_perm = w.at<float>(L.y_perm);
   if ((st = run_experts(*d, rows_src, table, experts, shared, kEpiStoreRows, nullptr, nullptr,
-                        y_perm, w, s, ev, xrows)) != MOE_OK)
+                        y_perm, w, s, ev, xrows, zero_gemm)) != MOE_OK)
     return st;
   const cudaError_t e = launch_combine(y_perm, w.at<int32_t>(L.row_of), wts, d->T, d->H,
                                        d->top_k, accumulate, out, s);

@@ -26,7 +26,8 @@ constexpr int kBK = 64;
 constexpr int kRowBytes = kBK * 2;  // 128
 constexpr int kATileBytes = kBM * kRowBytes;  // 16 KB per token plane
 constexpr int kStageBudget = 224 * 1024;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;     // + warp 6: token-row gather (idle unless gathering)
+constexpr int kGatherWarp = 6;
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -48,6 +49,11 @@ struct TmCfg {
 
 struct TmArgs {
   const int32_t* table;
+  const int32_t* arows;   // gate/up: non-null -> token row r is xsrc[arows[r]] (cp.async)
+  const uint16_t* xsrc;   // x [T][xpitch] bf16
+  int xpitch;
+  float4* zero_out;       // gate/up: cleared by the epilogue warps before their first tile
+  size_t zero_n4;
   int K, N_out, nblocks, E, total_rows, out_rows;
   const int32_t* gather;
   const float* roww;
@@ -98,9 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // gathered token rows: each of the producer warp's 32 lanes also arrives
+  const bool gat = NA == 1 && a.arows != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], gat ? 33 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -143,11 +151,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = tiles + stage * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          // gathered rows arrive through the gather warp, outside the tx count
+          mbar_arrive_expect_tx(&full[stage], gat ? Cfg::kStageBytes - kATileBytes : Cfg::kStageBytes);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          tma_load_2d(st, &tm_a0, &full[stage], kb * kBK, te.row0, pol_x);
-          if (NA == 2) tma_load_2d(st + kATileBytes, &tm_a1, &full[stage], kb * kBK, te.row0, pol_x);
+          if (!gat) {
+            tma_load_2d(st, &tm_a0, &full[stage], kb * kBK, te.row0, pol_x);
+            if (NA == 2)
+              tma_load_2d(st + kATileBytes, &tm_a1, &full[stage], kb * kBK, te.row0, pol_x);
+          }
           uint8_t* sb = st + NA * kATileBytes;
           tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &full[stage], kb * kBK, nb * FN, ge, pol_w);
           if (NBM == 2)
@@ -205,7 +217,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
+  } else if (warp == kGatherWarp) {
+    if (gat) {
+      // Token rows gathered from x by cp.async, in the stage order of the TMA
+      // producer: eight lanes cover one 128-byte row (one 16-byte piece each,
+      // placed in the 128-byte swizzle the MMA reads), so one instruction
+      // copies four whole rows; rows past the group are left as they are
+      // (they reach only output rows the epilogue never writes).  Up to
+      // kDepth stages of copies stay in flight; for the oldest one every lane
+      // waits for its copies, fences the async proxy and arrives.
+      constexpr int kDepth = cmin(3, Cfg::kStages);
+      const int j = lane & 7;  // 16-byte piece of the row
+      int stage = 0, inflight = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      auto signal_oldest = [&]() {
+        fence_proxy_async_smem();
+        int so = stage - inflight;
+        if (so < 0) so += Cfg::kStages;
+        mbar_arrive(&full[so]);
+        --inflight;
+      };
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileEntry te = entry_at(a.table, tile / a.nblocks);
+        int tok[kBM / 4];  // token of row 4i + lane / 8
+#pragma unroll
+        for (int i = 0; i < kBM / 4; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          tok[i] = r < te.nrows ? a.arows[te.row0 + r] : 0;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, ab))) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + stage * Cfg::kStageBytes;
+#pragma unroll
+          for (int i = 0; i < kBM / 4; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            if (r < te.nrows)
+              cp_async_16(st + r * kRowBytes + ((j ^ (r & 7)) << 4),
+                          a.xsrc + static_cast<size_t>(tok[i]) * a.xpitch + kb * kBK + j * 8);
+          }
+          cp_async_commit();
+          ++inflight;
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (inflight == kDepth) {
+            cp_async_wait<kDepth - 1>();
+            signal_oldest();
+          }
+        }
+      }
+      cp_async_wait<0>();
+      while (inflight > 0) signal_oldest();
+    }
   } else {
+    // The layer output is cleared here when asked (only the down GEMM, a
+    // later launch, adds into it): the epilogue warps are otherwise idle
+    // until their first accumulator is ready.
+    if (a.zero_out) {
+      const size_t nthr = static_cast<size_t>(gridDim.x) * 128;
+      for (size_t i = static_cast<size_t>(blockIdx.x) * 128 + (threadIdx.x - 64); i < a.zero_n4; i += nthr)
+        a.zero_out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const int q = warp & 3;
     const int lrow = q * 32 + lane;  // token row of the tile this thread owns
     int acc = 0;
@@ -288,7 +365,8 @@ cudaError_t tm_dispatch(const TmLaunch& L, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  TmArgs a{L.table, L.K, L.N_out, L.nblocks, L.E, L.total_rows, L.out_rows,
+  TmArgs a{L.table, L.arows, static_cast<const uint16_t*>(L.xsrc), L.xpitch,
+           reinterpret_cast<float4*>(L.zero_out), L.zero_out ? L.zero_n / 4 : 0, L.K, L.N_out, L.nblocks, L.E, L.total_rows, L.out_rows,
            L.gather, L.roww, L.out, L.h0, L.h1, L.status, L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);

@@ -171,6 +171,11 @@ cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
 struct TmLaunch {
   CUtensorMap tm_a[2], tm_b[2], tm_sb[2];
   const int32_t* table;
+  const int32_t* arows;  // gate/up: non-null -> token row r is x[arows[r]], copied from
+  const void* xsrc;      // xsrc [T][xpitch] bf16 by the producer warp (tm_a[0] unused)
+  int xpitch;
+  float* zero_out;       // gate/up: zero_n floats the kernel clears (null: none)
+  size_t zero_n;
   bool gateup;
   int K, N_out, nblocks, E, total_rows, out_rows, epilogue;
   const int32_t* gather;

@@ -151,6 +151,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 16-byte copy global -> shared that bypasses L1 (cp.async); completion is
+// waited for per thread with cp_async_wait<N> (at most N younger commit
+// groups still pending).  Its shared-memory writes are generic-proxy writes:
+// a thread that hands them to tcgen05.mma fences the async proxy first.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // L2 eviction policies for TMA loads: streamed weights are read once
 // (evict_first); activations are re-read by the other tiles of their group
 // (evict_last).
