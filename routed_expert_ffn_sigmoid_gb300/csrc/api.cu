@@ -332,9 +332,9 @@ moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, co
   if (e == cudaSuccess)
     e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
   if (e == cudaSuccess && materialise)
-    e = launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(d), d.H, d.T,
-                           d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
-                           zero_out ? static_cast<size_t>(d.T) * d.H : 0, s);
+    e = launch_scatter_rows(static_cast<const uint16_t*>(x), row_of, d.T, d.H, d.top_k,
+                            d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
+                            zero_out ? static_cast<size_t>(d.T) * d.H : 0, s);
   return from_cuda(e);
 }
 
@@ -618,9 +618,9 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
     if (!fused && launch_small_permutation(idx, wts, d->T, d->E, d->top_k, perm, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rows_from_x &&
-        launch_gather_rows(static_cast<const uint16_t*>(x), gather, rows_of(*d), d->H, d->T, int4,
-                           static_cast<uint16_t*>(x_perm), zero_gather,
-                           zero_gather ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
+        launch_scatter_rows(static_cast<const uint16_t*>(x), w.at<int32_t>(L.row_of), d->T, d->H,
+                            d->top_k, int4, static_cast<uint16_t*>(x_perm), zero_gather,
+                            zero_gather ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
     if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather,
@@ -800,8 +800,8 @@ moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* we
     return MOE_ERR_CUDA;
   const void* rows = x;
   if (d->fmt == MOE_W_INT4_G32) {  // the Int4 GEMMs take fp16 activations
-    if (launch_gather_rows(static_cast<const uint16_t*>(x), gather, d->T, d->H, d->T, true,
-                           w.at<uint16_t>(w.L.x_perm), nullptr, 0, s) != cudaSuccess)
+    if (launch_scatter_rows(static_cast<const uint16_t*>(x), nullptr, d->T, d->H, 0, true,
+                            w.at<uint16_t>(w.L.x_perm), nullptr, 0, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     rows = w.at<void>(w.L.x_perm);
   }

@@ -72,12 +72,13 @@ cudaError_t launch_perm_scan(int32_t* blockcnt, int T, int E, int k, int32_t* of
 cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_t* blockbase,
                                 int T, int E, int k, int32_t* gather, int32_t* row_of,
                                 float* roww, cudaStream_t s);
-// x_perm[r] = x[gather[r]]; to_fp16 converts bf16 -> fp16 on the way.  When
-// zero_out is not null the kernel also zeroes zero_n floats there (a multiple
-// of 4, 16-byte aligned).
-cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
-                               bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
-                               cudaStream_t s);
+// x_perm[row_of[t][j]] = x[t] for j < k and x_perm[k*T + t] = x[t] (the
+// shared row; k = 0: x_perm = x), in token order; to_fp16 converts bf16 ->
+// fp16 in the Int4 operand order on the way.  When zero_out is not null the
+// kernel also zeroes zero_n floats there (a multiple of 4, 16-byte aligned).
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
+                                bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
+                                cudaStream_t s);
 // Dense FFN: rows 0..T-1 are one group (group 0): gather[r] = r, roww[r] = 1
 // and a tile table of ceil(T / BN) entries.
 cudaError_t launch_dense_rows(int T, int BN, int32_t* gather, float* roww, int32_t* table,

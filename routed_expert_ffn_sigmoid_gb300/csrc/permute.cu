@@ -13,6 +13,8 @@
 //   4. x rows are gathered into permuted order with 16-byte loads.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "moe_kernels.h"
 #include "ptx.cuh"
 #include "route_common.cuh"
@@ -140,16 +142,21 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
   }
 }
 
-// One warp per row, grid-stride.  H is a multiple of 128, so a row is a whole
-// number of 16-byte chunks.  When zero_out is set, the kernel also clears the
-// layer output (zero_n floats) that the down kernel later adds into.
+// Token rows into x_perm, one warp per (token, column segment), grid-stride:
+// each piece of x[t] is read once and written to the token's k routed rows
+// (row_of[t][j]) and to its shared row k*T + t -- in token order, so each
+// source row crosses HBM once even when x is larger than L2 (a copy in row
+// order re-reads it up to k+1 times); `segs` segments per row keep enough
+// warps busy when T is small.  H is a multiple of 128, so a row is a whole
+// number of 16-byte chunks.  When zero_out is set, the kernel also clears
+// the layer output (zero_n4 float4s) that the down kernel later adds into.
 template <bool kToFp16>
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ gather,
-                                                          int rows, int H, int T,
-                                                          uint16_t* __restrict__ x_perm,
-                                                          float4* __restrict__ zero_out,
-                                                          size_t zero_n4) {
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __restrict__ x,
+                                                           const int32_t* __restrict__ row_of,
+                                                           int T, int H, int k, int segs,
+                                                           uint16_t* __restrict__ x_perm,
+                                                           float4* __restrict__ zero_out,
+                                                           size_t zero_n4) {
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
   if (zero_out) {
@@ -160,14 +167,18 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int chunks = H / 8;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-    const int t = gather[r];
-    const bool valid = t >= 0 && t < T;  // rows no pair claimed stay zero
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(valid ? t : 0) * H);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
-    for (int c = lane; c < chunks; c += 32) {
-      uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  const int seg_chunks = H / 8 / segs;
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * segs; item += warps) {
+    const int t = item / segs, c0 = (item % segs) * seg_chunks;
+    uint4* dst[kMaxTopK + 1];
+#pragma unroll
+    for (int j = 0; j <= kMaxTopK; ++j) {
+      const int r = j < k ? row_of[static_cast<size_t>(t) * k + j] : k * T + t;
+      dst[j] = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    for (int c = c0 + lane; c < c0 + seg_chunks; c += 32) {
+      uint4 v = __ldg(src + c);
       if (kToFp16) {
         // exact bf16 -> fp16, the 8 columns stored in the Int4 kernels'
         // operand order 0, 4, 1, 5, 2, 6, 3, 7
@@ -186,7 +197,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
         }
         v = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      dst[c] = v;
+#pragma unroll
+      for (int j = 0; j <= kMaxTopK; ++j)
+        if (j <= k) dst[j][c] = v;
     }
   }
 }
@@ -274,18 +287,25 @@ cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_
                     0, s, idx, w, blockbase, T, E, k, gather, row_of, roww);
 }
 
-cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* gather, int rows, int H, int T,
-                               bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
-                               cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  const int blocks = min((rows + 7) / 8, 152 * 8);
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
+                                bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
+                                cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (k < 0 || k > kMaxTopK) return cudaErrorInvalidValue;
+  // column segments per row: at least 32 chunks each, about 1216 warps in all
+  const int chunks = H / 8;
+  int segs = 1;
+  while (segs < 16 && static_cast<long>(T) * segs < 152 * 8 && chunks % (segs * 2 * 32) == 0)
+    segs *= 2;
+  const long items = static_cast<long>(T) * segs;
+  const int blocks = static_cast<int>(std::min<long>((items + 7) / 8, 152 * 8));
   float4* z4 = reinterpret_cast<float4*>(zero_out);
   const size_t n4 = zero_n / 4;
   if (to_fp16)
-    return launch_pdl(gather_rows_kernel<true>, dim3(blocks), dim3(256), 0, s, x, gather, rows, H,
-                      T, x_perm, z4, n4);
-  return launch_pdl(gather_rows_kernel<false>, dim3(blocks), dim3(256), 0, s, x, gather, rows, H,
-                    T, x_perm, z4, n4);
+    return launch_pdl(scatter_rows_kernel<true>, dim3(blocks), dim3(256), 0, s, x, row_of, T, H, k,
+                      segs, x_perm, z4, n4);
+  return launch_pdl(scatter_rows_kernel<false>, dim3(blocks), dim3(256), 0, s, x, row_of, T, H, k,
+                    segs, x_perm, z4, n4);
 }
 
 cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,
