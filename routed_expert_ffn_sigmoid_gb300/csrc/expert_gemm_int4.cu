@@ -427,6 +427,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileEntry te = entry_at(a.table, tile / a.mblocks);
       const int mb = tile % a.mblocks;
+      // Scatter-add: the tile's token ids and routing weights (nrows <= BN
+      // <= 128), loaded while its MMAs run -- lane l holds rows l, l + 32,
+      // l + 64, l + 96 -- so the atomics below wait on no global load.
+      int tk[4] = {-1, -1, -1, -1};
+      float tw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (NA == 1 && EPI == kEpiScatterAdd) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = j * 32 + lane;
+          const int rr = te.row0 + i;
+          if (i < te.nrows && rr < a.total_rows) {
+            const int t = a.gather[rr];
+            tw[j] = a.roww[rr];
+            tk[j] = (t >= 0 && t < a.out_rows) ? t : -1;
+          }
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
       tc_fence_after_sync();
       const int f = mb * kBM + q * 32 + lane;
@@ -450,12 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x0 = __uint_as_float(v0[4 * g]), x1 = __uint_as_float(v0[4 * g + 1]);
             float x2 = __uint_as_float(v0[4 * g + 2]), x3 = __uint_as_float(v0[4 * g + 3]);
             transpose4_lanes(x0, x1, x2, x3, lane);
-            const int c = c0 + 4 * g + r4;
-            const int rr = te.row0 + c;
-            if (c < te.nrows && rr < a.total_rows && f < a.N_out) {
-              const int t = a.gather[rr];
-              if (t >= 0 && t < a.out_rows) {
-                const float wr = a.roww[rr];
+            const int cb = c0 + 4 * g;  // a multiple of 4: the same register slot for all lanes
+            const int j = cb >> 5;
+            const int src = (cb + r4) & 31;
+            const int t = __shfl_sync(
+                0xffffffffu, j == 0 ? tk[0] : j == 1 ? tk[1] : j == 2 ? tk[2] : tk[3], src);
+            const float wr = __shfl_sync(
+                0xffffffffu, j == 0 ? tw[0] : j == 1 ? tw[1] : j == 2 ? tw[2] : tw[3], src);
+            const int c = cb + r4;
+            if (c < te.nrows && f < a.N_out) {
+              if (t >= 0) {
                 atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(t) * a.N_out),
                           make_float4(wr * x0, wr * x1, wr * x2, wr * x3));
               }

@@ -290,9 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileEntry te = entry_at(a.table, tile / a.nblocks);
       const int nb = tile % a.nblocks;
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
-      tc_fence_after_sync();
-      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
+      // this thread's token id and weight, loaded while the tile's MMAs run
       const int r = te.row0 + lrow;
       const bool valid = lrow < te.nrows && r < a.total_rows;
       int t = 0;
@@ -301,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         t = a.gather[r];
         wr = a.roww[r];
       }
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
+      tc_fence_after_sync();
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
       const bool live = valid && (EPI != kEpiScatterAdd || (t >= 0 && t < a.out_rows));
       for (int c0 = 0; c0 < FN; c0 += 16) {
         uint32_t v0[16], v1[16];

@@ -139,3 +139,25 @@ def test_forward_int4_forced_overflow(decode4):
     sample = np.arange(0, T, 29)
     ref, idx, _ = oracle.moe_forward(x[sample], inp.w_router, b, inp.experts, inp.shared, "int4")
     assert rel_max_err(out[sample], ref) <= TOL["int4"]
+
+
+def test_skewed_prefill_scatter_add_matches_deterministic(skewed4):
+    # Full size, every element: the atomic scatter-add of the down
+    # projection (token ids and weights held in registers per tile) against
+    # the deterministic mode's stored rows and fixed-order combination.  They
+    # agree up to fp32 summation order only if every (token, slot) row lands
+    # exactly once with its weight.
+    x = skewed4.inp.x
+    wl = skewed4.wl
+    outs = []
+    for flags in (0, moe.MOE_FLAG_DETERMINISTIC):
+        dims = moe.make_dims(x.shape[0], wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, flags)
+        ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+        out = torch.full((x.shape[0], wl.H), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(dims, dev_u16(x), skewed4.wr, skewed4.b, skewed4.exw, skewed4.shw,
+                            out, ws)
+        assert moe.moe_workspace_status(ws) == moe.MOE_OK
+        outs.append(out.cpu().numpy())
+        del ws, out
+    assert np.all(np.isfinite(outs[0]))
+    assert rel_max_err(outs[0], outs[1]) <= 1e-5

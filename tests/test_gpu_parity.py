@@ -278,3 +278,23 @@ def test_unsupported_shapes_are_rejected(tiny):
         moe.moe_ffn_forward(dims, dev_u16(np.zeros((8, 200), np.uint16)), tiny.wr, tiny.b,
                             tiny.exw, tiny.shw, out, ws)
     assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_prefill_8192_scatter_add_matches_deterministic(prefill):
+    # 8192 tokens, every element: the token-major kernels' atomic
+    # scatter-add against the deterministic mode's stored rows and
+    # fixed-order combination, equal up to fp32 summation order.
+    wl = prefill.wl
+    x = synthetic.gen_x(wl, T=8192)
+    outs = []
+    for flags in (0, moe.MOE_FLAG_DETERMINISTIC):
+        dims = moe.make_dims(8192, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, flags)
+        ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+        out = torch.full((8192, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(dims, dev_u16(x), prefill.wr, prefill.b, prefill.exw, prefill.shw,
+                            out, ws)
+        assert moe.moe_workspace_status(ws) == moe.MOE_OK
+        outs.append(out.cpu().numpy())
+        del ws, out
+    assert np.all(np.isfinite(outs[0]))
+    assert rel_max_err(outs[0], outs[1]) <= 1e-5
