@@ -225,7 +225,12 @@ def config_of(wl, world, args=None):
             "x_batches_cycled": N_BATCHES,
             "l2": "flushed before every step (512 MB write); weights read per step exceed L2",
             "launch": ("eager layer calls" if args is not None and args.eager else
-                       "CUDA graph replay, one captured layer call per x batch"),
+                       "CUDA graph replay, one captured layer call per x batch, timed by "
+                       "events around each replay"),
+            "stage_split": ("events between the stages of each call" if args is not None
+                            and args.eager else
+                            "second pass of K replays of graphs with event nodes between the "
+                            "stages (gate/up duration for the roofline)"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -340,30 +345,47 @@ def run_ours(args, wl, rank, world, local):
         stage_ms = [[evs[i].elapsed_time(evs[i + 1]) for evs, _ in step_events]
                     for i in range(nst)]
     else:
-        # One graph per x batch: the layer call (all its kernels and stage
-        # events) captured once, replayed every step; the L2 flush runs
-        # between replays, outside the graphs.
-        graphs = []
+        # One graph per x batch: the layer call (all its kernels) captured
+        # once, replayed every step, timed by events recorded on the stream
+        # around the replay; the L2 flush runs between replays, outside the
+        # graphs.  A second pass of K replays times the stages with graphs
+        # of moe_ffn_forward_timed: their event nodes between the kernels
+        # keep each kernel from starting early (programmatic dependent
+        # launch), which costs ~13 us per step at 1-8 tokens, so that pass
+        # gives the stage split and the kernel durations, not the step time.
+        graphs, staged = [], []
         cap = torch.cuda.Stream(dev)
         for bi in range(N_BATCHES):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                moe.moe_ffn_forward(dims, xs[bi], wr, b, exw, shw, out, ws)
+            graphs.append(g)
             evs, se = new_events()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
                 moe.moe_ffn_forward_timed(dims, xs[bi], wr, b, exw, shw, out, ws, se)
-            graphs.append((g, evs))
+            staged.append((g, evs))
         for s in range(args.warmup):
-            graphs[s % N_BATCHES][0].replay()
+            graphs[s % N_BATCHES].replay()
+            staged[s % N_BATCHES][0].replay()
         torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         step_ms, stage_ms = [], [[] for _ in range(nst)]
         with ClockSampler(local) as clk:
             time.sleep(0.3)
             for s in range(args.steps):
                 flush.zero_()
-                g, evs = graphs[s % N_BATCHES]
+                e0.record(stream)
+                graphs[s % N_BATCHES].replay()
+                e1.record(stream)
+                e1.synchronize()
+                step_ms.append(e0.elapsed_time(e1))
+            for s in range(args.steps):
+                flush.zero_()
+                g, evs = staged[s % N_BATCHES]
                 g.replay()
                 # the graph's events are read before the graph runs again
                 torch.cuda.synchronize(dev)
-                step_ms.append(evs[0].elapsed_time(evs[nst]))
                 for i in range(nst):
                     stage_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
     if world > 1:
