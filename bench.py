@@ -92,11 +92,13 @@ def gateup_bytes(wl, distinct):
 def gateup_traffic_per_launch(wl, units):
     """DRAM bytes of one gate/up launch from the committed ncu capture
     (profiles/gateup_traffic.json), scaled by the expert units processed;
-    None when the kernel source changed since the capture or the workload
-    shape differs."""
+    None when the kernel source changed since the capture, the workload
+    shape differs, or the launch runs another kernel (above 64 tokens the
+    token-major kernel serves gate/up)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "gateup_traffic.json")
-    if not os.path.exists(p) or wl.fmt != "bf16" or (wl.H, wl.I) != (4096, 1536):
+    if (not os.path.exists(p) or wl.fmt != "bf16" or (wl.H, wl.I) != (4096, 1536)
+            or wl.T > 64):
         return None
     with open(p) as f:
         rec = json.load(f)

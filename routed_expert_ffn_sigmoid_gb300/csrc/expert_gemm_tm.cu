@@ -10,9 +10,13 @@
 // down projection, and the epilogue owns one token row per thread, so h is
 // written with 16-byte stores and the output with 16-byte vector atomics.
 //
-// CTA = 6 warps (TMA producer, MMA issuer, 4 epilogue warps), persistent over
-// (tile-table entry, feature block) pairs, accumulators double-buffered in
-// TMEM, every wait bounded as in the other GEMM kernels.
+// CTA = 7 warps (weight producer, MMA issuer, 4 epilogue warps, token
+// producer), persistent over (tile-table entry, feature block) pairs,
+// accumulators double-buffered in TMEM, every wait bounded as in the other
+// GEMM kernels.  Weight tiles (from HBM) and token planes (mostly L2 hits)
+// have rings of their own, so their depths are set apart: the down
+// projection's two 16 KB token planes per K step no longer limit its weight
+// ring to three stages (96 KB of HBM bytes in flight per SM; now 128 KB).
 #include <cuda_bf16.h>
 
 #include "moe_kernels.h"
@@ -25,9 +29,8 @@ constexpr int kBM = 128;            // token rows per tile
 constexpr int kBK = 64;
 constexpr int kRowBytes = kBK * 2;  // 128
 constexpr int kATileBytes = kBM * kRowBytes;  // 16 KB per token plane
-constexpr int kStageBudget = 224 * 1024;
-constexpr int kThreads = 224;     // + warp 6: token-row gather (idle unless gathering)
-constexpr int kGatherWarp = 6;
+constexpr int kThreads = 224;
+constexpr int kGatherWarp = 6;    // token producer: TMA, or cp.async rows gathered from x
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -36,15 +39,23 @@ __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 template <int NA, int NBM, int FN>
 struct TmCfg {
   static constexpr int kBTileBytes = FN * kRowBytes;
-  static constexpr int kStageBytes = NA * kATileBytes + NBM * kBTileBytes;
-  static constexpr int kStages = cmin(6, kStageBudget / kStageBytes);
+  static constexpr int kAStageBytes = NA * kATileBytes;  // token planes of one K step
+  static constexpr int kBStageBytes = NBM * kBTileBytes; // weight tiles of one K step
+  // Measured at 1024-8192 tokens and on the dense FFN: gate/up is best with
+  // 4 + 4 stages (fewer token stages, or a fifth weight stage, cost 10-35 %),
+  // down with 3 + 4 (5-8 % faster than three shared stages of both).
+  static constexpr int kAStages = NA == 2 ? 3 : 4;
+  static constexpr int kBStages = 4;
   static constexpr int kAccCols = NBM * FN;  // 256 in both uses
   static constexpr int kAccStages = 2;
   static constexpr int kTmemCols = 512;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static constexpr int kSmemBytes =
+      kAStages * kAStageBytes + kBStages * kBStageBytes + 1024 + 256;
   static_assert(kAccStages * kAccCols <= 512, "TMEM");
   static_assert(NBM * FN <= 256, "one MMA spans every weight tile of a stage");
-  static_assert(kStageBytes % 1024 == 0, "alignment");
+  static_assert(kAStageBytes % 1024 == 0 && kBStageBytes % 1024 == 0, "alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kAStages + kBStages <= 16, "rings");
 };
 
 struct TmArgs {
@@ -94,22 +105,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_sb1, const TmArgs a) {
   using Cfg = TmCfg<NA, NBM, FN>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* tiles = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + Cfg::kStages * Cfg::kStageBytes);
-  uint64_t* empty = full + Cfg::kStages;
-  uint64_t* tfull = empty + Cfg::kStages;
+  uint8_t* aring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* bring = aring + Cfg::kAStages * Cfg::kAStageBytes;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(bring + Cfg::kBStages * Cfg::kBStageBytes);
+  uint64_t* a_empty = a_full + Cfg::kAStages;
+  uint64_t* b_full = a_empty + Cfg::kAStages;
+  uint64_t* b_empty = b_full + Cfg::kBStages;
+  uint64_t* tfull = b_empty + Cfg::kBStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // gathered token rows: each of the producer warp's 32 lanes also arrives
+  // gathered token rows: each lane of the token producer warp arrives
   const bool gat = NA == 1 && a.arows != nullptr;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&full[s], gat ? 33 : 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < Cfg::kAStages; ++s) {
+      mbar_init(&a_full[s], gat ? 32 : 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < Cfg::kBStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -135,8 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = a.K / kBK;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- weight producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      const uint64_t pol_w = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
@@ -146,33 +165,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool sh = te.group == a.E;
         const int ge = sh ? 0 : te.group;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, ab)) {
+          if (!mbar_wait(&b_empty[stage], phase ^ 1u, ab)) {
             ok = false;
             break;
           }
-          uint8_t* st = tiles + stage * Cfg::kStageBytes;
-          // gathered rows arrive through the gather warp, outside the tx count
-          mbar_arrive_expect_tx(&full[stage], gat ? Cfg::kStageBytes - kATileBytes : Cfg::kStageBytes);
+          uint8_t* sb = bring + stage * Cfg::kBStageBytes;
+          mbar_arrive_expect_tx(&b_full[stage], Cfg::kBStageBytes);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (!gat) {
-            tma_load_2d(st, &tm_a0, &full[stage], kb * kBK, te.row0, pol_x);
-            if (NA == 2)
-              tma_load_2d(st + kATileBytes, &tm_a1, &full[stage], kb * kBK, te.row0, pol_x);
-          }
-          uint8_t* sb = st + NA * kATileBytes;
-          tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &full[stage], kb * kBK, nb * FN, ge, pol_w);
+          tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &b_full[stage], kb * kBK, nb * FN, ge, pol_w);
           if (NBM == 2)
-            tma_load_3d(sb + Cfg::kBTileBytes, sh ? &tm_sb1 : &tm_b1, &full[stage], kb * kBK,
+            tma_load_3d(sb + Cfg::kBTileBytes, sh ? &tm_sb1 : &tm_b1, &b_full[stage], kb * kBK,
                         nb * FN, ge, pol_w);
-          if (++stage == Cfg::kStages) {
+          if (++stage == Cfg::kBStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      for (int s = 0; s < Cfg::kStages; ++s)
-        if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_par >> s) & 1u);
+      for (int s = 0; s < Cfg::kBStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&b_full[s], (armed_par >> s) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -180,33 +192,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one N = 256 MMA covers both (columns 0..127 gate, 128..255 up) and
       // reads each token tile once per K step instead of twice
       const uint32_t idesc = idesc_f16(kBM, NBM * FN, true);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int sa = 0, sbs = 0, acc = 0;
+      uint32_t pa = 0, pb = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ab)) break;
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + acc * Cfg::kAccCols;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[stage], phase, ab)) {
+          if (!mbar_wait(&b_full[sbs], pb, ab) || !mbar_wait(&a_full[sa], pa, ab)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t st = smem_u32(tiles + stage * Cfg::kStageBytes);
+          const uint32_t st = smem_u32(aring + sa * Cfg::kAStageBytes);
           const uint64_t da0 = sw128_kmajor_desc(st);
           const uint64_t da1 = sw128_kmajor_desc(st + kATileBytes);
-          const uint64_t db0 = sw128_kmajor_desc(st + NA * kATileBytes);
+          const uint64_t db0 = sw128_kmajor_desc(smem_u32(bring + sbs * Cfg::kBStageBytes));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accum = (kb | k) != 0;
             umma_f16(d0, da0 + 2 * k, db0 + 2 * k, idesc, accum);
             if (NA == 2) umma_f16(d0, da1 + 2 * k, db0 + 2 * k, idesc, 1u);
           }
-          umma_commit(&empty[stage]);
-          if (++stage == Cfg::kStages) {
-            stage = 0;
-            phase ^= 1u;
+          umma_commit(&a_empty[sa]);
+          umma_commit(&b_empty[sbs]);
+          if (++sa == Cfg::kAStages) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sbs == Cfg::kBStages) {
+            sbs = 0;
+            pb ^= 1u;
           }
         }
         if (!ok) break;
@@ -218,7 +235,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(drain, 0);
     }
   } else if (warp == kGatherWarp) {
-    if (gat) {
+    if (!gat) {
+      // ---------------------------------------------------------------- token producer (TMA)
+      if (lane == 0) {
+        const uint64_t pol_x = policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_par = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+          const TileEntry te = entry_at(a.table, tile / a.nblocks);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&a_empty[stage], phase ^ 1u, ab)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = aring + stage * Cfg::kAStageBytes;
+            mbar_arrive_expect_tx(&a_full[stage], Cfg::kAStageBytes);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            tma_load_2d(st, &tm_a0, &a_full[stage], kb * kBK, te.row0, pol_x);
+            if (NA == 2)
+              tma_load_2d(st + kATileBytes, &tm_a1, &a_full[stage], kb * kBK, te.row0, pol_x);
+            if (++stage == Cfg::kAStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        for (int s = 0; s < Cfg::kAStages; ++s)
+          if ((armed >> s) & 1u) mbar_wait_drain(&a_full[s], (armed_par >> s) & 1u);
+      }
+    } else {
       // Token rows gathered from x by cp.async, in the stage order of the TMA
       // producer: eight lanes cover one 128-byte row (one 16-byte piece each,
       // placed in the 128-byte swizzle the MMA reads), so one instruction
@@ -226,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (they reach only output rows the epilogue never writes).  Up to
       // kDepth stages of copies stay in flight; for the oldest one every lane
       // waits for its copies, fences the async proxy and arrives.
-      constexpr int kDepth = cmin(3, Cfg::kStages);
+      constexpr int kDepth = cmin(3, Cfg::kAStages);
       const int j = lane & 7;  // 16-byte piece of the row
       int stage = 0, inflight = 0;
       uint32_t phase = 0;
@@ -234,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto signal_oldest = [&]() {
         fence_proxy_async_smem();
         int so = stage - inflight;
-        if (so < 0) so += Cfg::kStages;
-        mbar_arrive(&full[so]);
+        if (so < 0) so += Cfg::kAStages;
+        mbar_arrive(&a_full[so]);
         --inflight;
       };
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -247,11 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok[i] = r < te.nrows ? a.arows[te.row0 + r] : 0;
         }
         for (int kb = 0; kb < KB; ++kb) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, ab))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[stage], phase ^ 1u, ab))) {
             ok = false;
             break;
           }
-          uint8_t* st = tiles + stage * Cfg::kStageBytes;
+          uint8_t* st = aring + stage * Cfg::kAStageBytes;
 #pragma unroll
           for (int i = 0; i < kBM / 4; ++i) {
             const int r = 4 * i + (lane >> 3);
@@ -261,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           cp_async_commit();
           ++inflight;
-          if (++stage == Cfg::kStages) {
+          if (++stage == Cfg::kAStages) {
             stage = 0;
             phase ^= 1u;
           }
