@@ -26,7 +26,8 @@ constexpr int kTmGatherMinTokens = 512;     // token-major gate/up copies its to
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t z, idx, w, blockcnt, offsets, table, gather, row_of, roww, x_perm, h0, h1, y_perm;
+  size_t z, idx, w, blockcnt, offsets, table, table2, gather, row_of, roww, x_perm, xinv, h0, h1,
+      y_perm;
   size_t partial, counters;
   size_t partial_units;  // K-split units the partial buffer holds (0: no split possible)
   size_t total;
@@ -44,10 +45,18 @@ int pick_bn(int T) {
   return 128;
 }
 
+// Int4 weights up to 64 tokens: gate/up on 8-bit operands (entries of at
+// most kF8MaxRows rows), down on the fp16 path over the same entries.
+bool int4_f8(const moe_dims& d) { return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0; }
+
+// Rows per tile-table entry of the fused layer.
+int table_bn(const moe_dims& d) { return int4_f8(d) ? kF8MaxRows : pick_bn(d.T); }
+
 size_t table_bytes(const moe_dims& d) {
-  // every group contributes at most ceil(cnt / 16) entries; the sum is
-  // bounded by (E + 1) + rows / 16
-  const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 15) / 16;
+  // every group contributes at most ceil(cnt / 8) entries (entries have at
+  // least 8 rows but the last of a group); the sum is bounded by
+  // (E + 1) + rows / 8
+  const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 7) / 8;
   return kTableHeaderBytes + entries * sizeof(TileEntry);
 }
 
@@ -100,10 +109,12 @@ Layout layout_of(const moe_dims& d) {
   L.blockcnt = take(nblk * E * 4);
   L.offsets = take((E + 2) * 4);
   L.table = take(table_bytes(d));
+  L.table2 = take(int4_f8(d) ? table_bytes(d) : 0);  // down entries of the 8-bit gate/up path
   L.gather = take(rows * 4);
   L.row_of = take(T * k * 4);
   L.roww = take(rows * 4);
-  L.x_perm = take(rows * H * 2);
+  L.x_perm = take(rows * H * 2);  // Int4 up to 64 tokens: the two e4m3 planes of each row
+  L.xinv = take(int4_f8(d) ? rows * 4 : 0);
   L.h0 = take(rows * I * 2);
   L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
   L.y_perm = take((d.flags & MOE_FLAG_DETERMINISTIC) ? rows * H * 4 : 0);
@@ -234,6 +245,20 @@ bool encode_scales(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 token planes of `rows` permuted rows, [2 rows][K] bytes (row 2r: hi,
+// 2r + 1: lo): box {128 bytes, 16 rows}, 128-byte swizzle.
+bool encode_e4m3_planes(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {K, 2 * rows};
+  const cuuint64_t strides[1] = {K};
+  const cuuint32_t box[2] = {128, 16};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool weights_ok(const moe_weights* w, int fmt) {
   if (!w || !w->gate || !w->up || !w->down) return false;
   if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return false;
@@ -357,10 +382,75 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
                        const moe_weights* ex, const moe_weights* sh, int epilogue,
                        const int32_t* gather, const float* roww, float* out, const Ws& ws,
                        cudaStream_t s, const moe_stage_events* ev = nullptr,
-                       const int32_t* xrows = nullptr, float* zero_out = nullptr) {
+                       const int32_t* xrows = nullptr, float* zero_out = nullptr,
+                       const float* xinv = nullptr, const int32_t* down_table = nullptr) {
   const int rows = rows_of(d);
-  const int BN = pick_bn(d.T);
   const int nsm = sm_count();
+  if (d.fmt == MOE_W_INT4_G32 && xinv && down_table) {
+    // 8-bit gate/up: x_perm holds the e4m3 planes, entries of <= 8 rows
+    const int max_entries = (d.E + 1) + (rows + kF8MaxRows - 1) / kF8MaxRows;
+    Int4F8Launch G{};
+    if (!encode_codes(&G.tm_c[0], ex->gate, d.H, d.I, d.E) ||
+        !encode_codes(&G.tm_c[1], ex->up, d.H, d.I, d.E) ||
+        !encode_codes(&G.tm_sc[0], sh->gate, d.H, d.I, 1) ||
+        !encode_codes(&G.tm_sc[1], sh->up, d.H, d.I, 1) ||
+        !encode_e4m3_planes(&G.tm_b, x_perm, d.H, rows))
+      return MOE_ERR_CUDA;
+    G.table = table;
+    G.K = d.H;
+    G.N_out = d.I;
+    G.E = d.E;
+    G.total_rows = rows;
+    G.gate_scale = ex->gate_scale;
+    G.up_scale = ex->up_scale;
+    G.sgate_scale = sh->gate_scale;
+    G.sup_scale = sh->up_scale;
+    G.xinv = xinv;
+    G.h = ws.at<void>(ws.L.h0);
+    G.status = ws.status();
+    G.budget_ns = kWaitBudgetNs;
+    const int gtiles = max_entries * (d.I / 128);
+    G.grid = gtiles < nsm ? gtiles : nsm;
+    record(ev, 2, s);
+    if (launch_int4_f8_gateup(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(ev, 3, s);
+    Int4Launch D{};
+    if (!encode_codes(&D.tm_c[0], ex->down, d.I, d.H, d.E) ||
+        !encode_scales(&D.tm_s[0], ex->down_scale, d.I, d.H, d.E) ||
+        !encode_codes(&D.tm_sc[0], sh->down, d.I, d.H, 1) ||
+        !encode_scales(&D.tm_ss[0], sh->down_scale, d.I, d.H, 1) ||
+        !encode_kmajor(&D.tm_b, G.h, false, d.I, rows, 1, 16))
+      return MOE_ERR_CUDA;
+    D.tm_c[1] = D.tm_c[0];
+    D.tm_s[1] = D.tm_s[0];
+    D.tm_sc[1] = D.tm_sc[0];
+    D.tm_ss[1] = D.tm_ss[0];
+    // down: its own table, entries of up to pick_bn rows (the shared
+    // expert's rows are not cut into 8-row pieces there)
+    const int dbn = pick_bn(d.T);
+    const int dmax_entries = (d.E + 1) + (rows + dbn - 1) / dbn;
+    D.table = down_table;
+    D.BN = dbn;
+    D.na = 1;
+    D.K = d.I;
+    D.N_out = d.H;
+    D.mblocks = d.H / 128;
+    D.E = d.E;
+    D.total_rows = rows;
+    D.out_rows = d.T;
+    D.epilogue = epilogue;
+    D.gather = gather;
+    D.roww = roww;
+    D.out = out;
+    D.status = ws.status();
+    D.budget_ns = kWaitBudgetNs;
+    const int dtiles = dmax_entries * D.mblocks;
+    D.grid = dtiles < nsm ? dtiles : nsm;
+    const cudaError_t e = launch_int4_gemm(D, s);
+    record(ev, 4, s);
+    return from_cuda(e);
+  }
+  const int BN = pick_bn(d.T);
   const int max_entries = (d.E + 1) + (rows + BN - 1) / BN;
   if (d.fmt == MOE_W_INT4_G32) {
     Int4Launch G{};
@@ -593,8 +683,11 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   // cost the copy engine more than the copy kernel, measured), and from
   // kTmGatherMinTokens tokens in the token-major kernels by cp.async from a
   // gather warp (measured: -3.1 % per step at 4096 tokens, -0.6 % at 512,
-  // +0.8 % at 128).  Int4 needs the fp16 copy in its operand order.
+  // +0.8 % at 128).  Int4 needs the fp16 copy in its operand order, or up
+  // to 64 tokens the two e4m3 planes of the 8-bit gate/up kernel.
   const bool int4 = d->fmt == MOE_W_INT4_G32;
+  const bool f8 = int4_f8(*d);
+  float* xinv = f8 ? w.at<float>(L.xinv) : nullptr;
   const bool tm = token_major(*d);
   const bool rows_from_x =
       !int4 && (d->T <= kGatherFromXTokens || (tm && d->T >= kTmGatherMinTokens));
@@ -606,8 +699,9 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   // decode sizes: one CTA permutes; up to kFusedPermTokens tokens it is the
   // top-k kernel's last CTA (one launch fewer), above a launch of its own
   // with more threads (measured faster at 64 tokens)
-  const SmallPermOut perm{w.route_done(), pick_bn(d->T), w.at<int32_t>(L.offsets), gather,
-                          w.at<int32_t>(L.row_of), roww, table};
+  int32_t* table2 = f8 ? w.at<int32_t>(L.table2) : nullptr;
+  const SmallPermOut perm{w.route_done(), table_bn(*d), w.at<int32_t>(L.offsets), gather,
+                          w.at<int32_t>(L.row_of), roww, table, table2, pick_bn(d->T)};
   const bool small = d->T <= kSmallT, fused = d->T <= kFusedPermTokens;
   record(ev, 0, s);
   if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s, zero_router,
@@ -617,11 +711,18 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   if (small) {
     if (!fused && launch_small_permutation(idx, wts, d->T, d->E, d->top_k, perm, s) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (!rows_from_x &&
-        launch_scatter_rows(static_cast<const uint16_t*>(x), w.at<int32_t>(L.row_of), d->T, d->H,
-                            d->top_k, int4, static_cast<uint16_t*>(x_perm), zero_gather,
-                            zero_gather ? static_cast<size_t>(d->T) * d->H : 0, s) != cudaSuccess)
+    const size_t zn = zero_gather ? static_cast<size_t>(d->T) * d->H : 0;
+    if (f8) {
+      if (launch_split_rows_e4m3(static_cast<const uint16_t*>(x), w.at<int32_t>(L.row_of), d->T,
+                                 d->H, d->top_k, static_cast<uint8_t*>(x_perm), xinv, zero_gather,
+                                 zn, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (!rows_from_x &&
+               launch_scatter_rows(static_cast<const uint16_t*>(x), w.at<int32_t>(L.row_of), d->T,
+                                   d->H, d->top_k, int4, static_cast<uint16_t*>(x_perm),
+                                   zero_gather, zn, s) != cudaSuccess) {
       return MOE_ERR_CUDA;
+    }
   } else {
     if ((st = run_permute(*d, idx, wts, x, w.at<int32_t>(L.offsets), gather,
                           w.at<int32_t>(L.row_of), roww, x_perm, table, w, s, zero_gather,
@@ -632,11 +733,11 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   const int32_t* xrows = rows_from_x ? gather : nullptr;
   if (!det)
     return run_experts(*d, rows_src, table, experts, shared, kEpiScatterAdd, gather, roww, out, w,
-                       s, ev, xrows, zero_gemm);
+                       s, ev, xrows, zero_gemm, xinv, table2);
   // deterministic: unweighted rows, then the fixed-order combination
   float* y_perm = w.at<float>(L.y_perm);
   if ((st = run_experts(*d, rows_src, table, experts, shared, kEpiStoreRows, nullptr, nullptr,
-                        y_perm, w, s, ev, xrows, zero_gemm)) != MOE_OK)
+                        y_perm, w, s, ev, xrows, zero_gemm, xinv, table2)) != MOE_OK)
     return st;
   const cudaError_t e = launch_combine(y_perm, w.at<int32_t>(L.row_of), wts, d->T, d->H,
                                        d->top_k, accumulate, out, s);

@@ -50,6 +50,8 @@ struct SmallPermOut {
   int32_t* row_of;
   float* roww;
   int32_t* table;
+  int32_t* table2;  // optional second tile table with entries of at most BN2 rows
+  int BN2;
 };
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
                                       int k, int32_t* idx, float* w, float* z,
@@ -79,6 +81,13 @@ cudaError_t launch_perm_scatter(const int32_t* idx, const float* w, const int32_
 cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
                                 bool to_fp16, uint16_t* x_perm, float* zero_out, size_t zero_n,
                                 cudaStream_t s);
+// The same copy of each token's row into its k + 1 permuted rows, as two
+// e4m3 planes under a power-of-two scale sigma per token (max |x sigma| in
+// [128, 256)): x8[2r][h] = e4m3(x sigma), x8[2r + 1][h] = e4m3(x sigma -
+// hi), xinv[r] = 1 / sigma.  Also clears zero_n floats of zero_out.
+cudaError_t launch_split_rows_e4m3(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
+                                   uint8_t* x8, float* xinv, float* zero_out, size_t zero_n,
+                                   cudaStream_t s);
 // Dense FFN: rows 0..T-1 are one group (group 0): gather[r] = r, roww[r] = 1
 // and a tile table of ceil(T / BN) entries.
 cudaError_t launch_dense_rows(int T, int BN, int32_t* gather, float* roww, int32_t* table,
@@ -164,6 +173,29 @@ struct Int4Launch {
   int grid;
 };
 cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
+
+// Int4 gate/up with the clamped SwiGLU on 8-bit operands (decode sizes):
+// codes n - 8 as e4m3 against the token rows as two e4m3 planes (hi, lo)
+// under a power-of-two scale per row; one MMA per scale group, scales
+// applied by the epilogue.  Tile entries hold at most 8 rows.
+constexpr int kF8MaxRows = 8;
+struct Int4F8Launch {
+  CUtensorMap tm_c[2];   // codes of the routed gate / up stacks
+  CUtensorMap tm_sc[2];  // codes of the shared expert's gate / up
+  CUtensorMap tm_b;      // e4m3 token planes: [2 rows][K] bytes, row 2r hi, 2r + 1 lo
+  const int32_t* table;
+  int K, N_out, E, total_rows;
+  const void* gate_scale;   // bf16 [E][N_out][K / 32]
+  const void* up_scale;
+  const void* sgate_scale;  // bf16 [1][N_out][K / 32]
+  const void* sup_scale;
+  const float* xinv;        // [rows] 1 / sigma of each token row
+  void* h;                  // fp16 [rows][N_out] in the Int4 operand order
+  int* status;
+  uint64_t budget_ns;
+  int grid;
+};
+cudaError_t launch_int4_f8_gateup(const Int4F8Launch& L, cudaStream_t s);
 
 // Token-major grouped GEMM (bf16, token tiles of 128 rows): gate/up with the
 // SwiGLU epilogue (h hi/lo planes) or down with the scatter-add / store-rows

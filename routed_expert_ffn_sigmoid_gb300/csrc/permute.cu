@@ -12,6 +12,7 @@
 //      the block's earlier tokens -> row = base + rank;
 //   4. x rows are gathered into permuted order with 16-byte loads.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 
@@ -204,6 +205,80 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
   }
 }
 
+// One CTA per token: the row maximum |x| gives sigma = 2^(8 - e) with
+// max = f 2^e, f in [0.5, 1), so max |x sigma| lies in [128, 256), inside
+// e4m3's range (448).  hi = e4m3(x sigma) and lo = e4m3(x sigma - hi),
+// both rounded to nearest by the hardware conversion; x sigma is exact (a
+// bf16 value times a power of two) and so is x sigma - hi in fp32.  The two
+// planes go to each of the token's k + 1 permuted rows.
+constexpr int kSplitThreads = 256;
+
+__global__ void __launch_bounds__(kSplitThreads) split_rows_e4m3_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ row_of, int T, int H, int k,
+    uint8_t* __restrict__ x8, float* __restrict__ xinv, float4* __restrict__ zero_out,
+    size_t zero_n4) {
+  __shared__ float s_max[kSplitThreads / 32];
+  __shared__ int32_t s_rows[kMaxTopK + 1];
+  pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  if (zero_out) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_n4;
+         i += stride)
+      zero_out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunks = H / 8;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    if (threadIdx.x <= k)
+      s_rows[threadIdx.x] =
+          threadIdx.x < k ? row_of[static_cast<size_t>(t) * k + threadIdx.x] : k * T + t;
+    float mx = 0.f;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv[i] << 16)),
+                             fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSplitThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    e = max(e, -100);  // a row of zeros (or tiny values) keeps a finite scale
+    const float sigma = ldexpf(1.0f, 8 - e);
+    if (threadIdx.x <= k) xinv[s_rows[threadIdx.x]] = 1.0f / sigma;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hi[2] = {0u, 0u}, lo[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y =
+            __uint_as_float((i & 1) ? (wv[i >> 1] & 0xFFFF0000u) : (wv[i >> 1] << 16)) * sigma;
+        const __nv_fp8_storage_t h8 = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+        const float hf = __half2float(__half(__nv_cvt_fp8_to_halfraw(h8, __NV_E4M3)));
+        const __nv_fp8_storage_t l8 = __nv_cvt_float_to_fp8(y - hf, __NV_SATFINITE, __NV_E4M3);
+        hi[i >> 2] |= static_cast<uint32_t>(h8) << (8 * (i & 3));
+        lo[i >> 2] |= static_cast<uint32_t>(l8) << (8 * (i & 3));
+      }
+      for (int j = 0; j <= k; ++j) {
+        uint8_t* rowp = x8 + static_cast<size_t>(s_rows[j]) * 2 * H;
+        reinterpret_cast<uint2*>(rowp)[c] = make_uint2(hi[0], hi[1]);
+        reinterpret_cast<uint2*>(rowp + H)[c] = make_uint2(lo[0], lo[1]);
+      }
+    }
+    __syncthreads();  // s_rows and s_max are rewritten for the next token
+  }
+}
+
 // Tile table from an offsets array (E+2 entries), one CTA.  Offsets are
 // clamped into [0, rows] and made non-decreasing, and no more than
 // `capacity` entries are written, so inconsistent offsets cannot send a tile
@@ -251,10 +326,11 @@ namespace {
 __global__ void __launch_bounds__(kSmallThreads) small_permutation_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int E, int k, int BN,
     int32_t* __restrict__ offsets, int32_t* __restrict__ gather, int32_t* __restrict__ row_of,
-    float* __restrict__ roww, int32_t* __restrict__ table) {
+    float* __restrict__ roww, int32_t* __restrict__ table, int32_t* __restrict__ table2,
+    int BN2) {
   pdl_wait();
   pdl_launch_dependents();  // dependents wait for this grid's completion themselves
-  small_permutation(idx, w, T, E, k, BN, offsets, gather, row_of, roww, table);
+  small_permutation(idx, w, T, E, k, BN, offsets, gather, row_of, roww, table, table2, BN2);
 }
 
 }  // namespace
@@ -263,7 +339,7 @@ cudaError_t launch_small_permutation(const int32_t* idx, const float* w, int T, 
                                      const SmallPermOut& p, cudaStream_t s) {
   if (T == 0 || T > kSmallT) return cudaErrorInvalidValue;
   return launch_pdl(small_permutation_kernel, dim3(1), dim3(kSmallThreads), 0, s, idx, w, T, E,
-                    k, p.BN, p.offsets, p.gather, p.row_of, p.roww, p.table);
+                    k, p.BN, p.offsets, p.gather, p.row_of, p.roww, p.table, p.table2, p.BN2);
 }
 
 cudaError_t launch_perm_count(const int32_t* idx, int T, int E, int k, int32_t* blockcnt,
@@ -306,6 +382,17 @@ cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_of, int T,
                       segs, x_perm, z4, n4);
   return launch_pdl(scatter_rows_kernel<false>, dim3(blocks), dim3(256), 0, s, x, row_of, T, H, k,
                     segs, x_perm, z4, n4);
+}
+
+cudaError_t launch_split_rows_e4m3(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
+                                   uint8_t* x8, float* xinv, float* zero_out, size_t zero_n,
+                                   cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (k > kMaxTopK || H % 8 != 0) return cudaErrorInvalidValue;
+  const int blocks = std::min(T, 1024);
+  float4* z4 = reinterpret_cast<float4*>(zero_out);
+  return launch_pdl(split_rows_e4m3_kernel, dim3(blocks), dim3(kSplitThreads), 0, s, x, row_of, T,
+                    H, k, x8, xinv, z4, zero_out ? zero_n / 4 : 0);
 }
 
 cudaError_t launch_table_from_offsets(const int32_t* offsets, int E, int rows, int capacity,

@@ -107,12 +107,35 @@ __device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) 
 // gather / row_of / row weights and the tile table -- the work of the count,
 // scan and scatter kernels with no launch in between.  The selection was
 // written by other CTAs of the calling grid: it is read past L1.
+__device__ __forceinline__ void write_tile_table(const int* off, int* ntile, int E, int BN,
+                                                 int* n_entries, int32_t* __restrict__ table) {
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (off[g + 1] - off[g] + BN - 1) / BN;
+  __syncthreads();
+  warp0_exclusive_scan(ntile, E + 1, n_entries);
+  __syncthreads();
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int o = off[g], c = off[g + 1] - o;
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      TileEntry te;
+      te.group = g;
+      te.row0 = o + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = *n_entries;
+}
+
 __device__ __forceinline__ void small_permutation(const int32_t* idx, const float* w, int T, int E,
                                                   int k, int BN, int32_t* __restrict__ offsets,
                                                   int32_t* __restrict__ gather,
                                                   int32_t* __restrict__ row_of,
                                                   float* __restrict__ roww,
-                                                  int32_t* __restrict__ table) {
+                                                  int32_t* __restrict__ table,
+                                                  int32_t* __restrict__ table2 = nullptr,
+                                                  int BN2 = 0) {
   __shared__ int s_idx[kSmallT * kMaxTopK];
   __shared__ float s_w[kSmallT * kMaxTopK];
   __shared__ int cnt[kMaxE + 2];
@@ -134,7 +157,6 @@ __device__ __forceinline__ void small_permutation(const int32_t* idx, const floa
   __syncthreads();
   if (threadIdx.x == 0) cnt[E] = T;
   __syncthreads();
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (cnt[g] + BN - 1) / BN;
   warp0_exclusive_scan(cnt, E + 1, &total_rows);  // cnt becomes the offsets
   __syncthreads();
   if (threadIdx.x == 0) cnt[E + 1] = total_rows;
@@ -153,21 +175,11 @@ __device__ __forceinline__ void small_permutation(const int32_t* idx, const floa
     gather[k * T + t] = t;
     roww[k * T + t] = 1.0f;
   }
-  warp0_exclusive_scan(ntile, E + 1, &n_entries);
-  __syncthreads();
-  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
-  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
-    const int o = cnt[g], c = cnt[g + 1] - o;
-    for (int i = 0, r = 0; r < c; ++i, r += BN) {
-      TileEntry te;
-      te.group = g;
-      te.row0 = o + r;
-      te.nrows = min(BN, c - r);
-      te.pad = 0;
-      ent[ntile[g] + i] = te;
-    }
+  write_tile_table(cnt, ntile, E, BN, &n_entries, table);
+  if (table2) {
+    __syncthreads();  // ntile is reused
+    write_tile_table(cnt, ntile, E, BN2, &n_entries, table2);
   }
-  if (threadIdx.x == 0) table[0] = n_entries;
 }
 
 // Launch helper: programmatic stream serialization lets a kernel begin while

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kMaxE) router_reduce_topk_kernel(
     if (s_last) {
       __threadfence();
       small_permutation(idx, w, T, E, k, perm.BN, perm.offsets, perm.gather, perm.row_of,
-                        perm.roww, perm.table);
+                        perm.roww, perm.table, perm.table2, perm.BN2);
       if (threadIdx.x == 0) *perm.done = 0;
     }
   }

@@ -161,3 +161,55 @@ def test_skewed_prefill_scatter_add_matches_deterministic(skewed4):
         del ws, out
     assert np.all(np.isfinite(outs[0]))
     assert rel_max_err(outs[0], outs[1]) <= 1e-5
+
+
+@pytest.mark.parametrize("T", [16, 17, 33])
+def test_forward_decode_int4_token_counts(decode4, T):
+    # Around the one-CTA permutation's boundaries (fused into the router up
+    # to 16 tokens); up to 64 tokens gate/up runs on 8-bit operands with tile
+    # entries of at most 8 rows and down on its own table.
+    x = decode4.inp.x[:T]
+    out = decode4.forward(x)
+    assert rel_max_err(out, _ref(decode4, x)) <= TOL["int4"]
+
+
+def test_forward_int4_all_tokens_one_expert_set_decode(decode4):
+    # 64 tokens all routed to the same 8 experts: every group has 64 rows,
+    # cut into 8 gate/up entries each, and into one down entry.
+    T = 64
+    x, _, _ = gapped_x(decode4.wl, decode4.inp.w_router, decode4.inp.b_router, T=T)
+    forced = [0, 5, 77, 100, 150, 201, 250, 287]
+    b = np.full(decode4.wl.E, -60.0, np.float32)
+    b[forced] = 60.0
+    saved = decode4.b
+    try:
+        decode4.b = torch.from_numpy(b).cuda()
+        out = decode4.forward(x)
+    finally:
+        decode4.b = saved
+    inp = decode4.inp
+    sample = np.arange(0, T, 7)
+    ref, idx, _ = oracle.moe_forward(x[sample], inp.w_router, b, inp.experts, inp.shared, "int4")
+    assert sorted(set(idx.ravel().tolist())) == forced
+    assert rel_max_err(out[sample], ref) <= TOL["int4"]
+
+
+def test_forward_int4_row_scales(decode4):
+    # The 8-bit path scales each token row by a power of two from its
+    # largest |x|: a row of zeros, rows of tiny and of large values, and a
+    # row with one large value among small ones, against the oracle.
+    T = 8
+    x = decode4.inp.x[:T].copy()
+    xf = synthetic.bf16_bits_to_f32(x)
+    xf[0] = 0.0
+    xf[1] *= 2.0 ** -60
+    xf[2] *= 2.0 ** 10
+    xf[3] *= 2.0 ** -12
+    xf[3, 17] = 3.0
+    rows = synthetic.f32_to_bf16_bits(xf)
+    out = decode4.forward(rows)
+    assert np.all(np.isfinite(out))
+    ref = _ref(decode4, rows)
+    assert rel_max_err(out, ref) <= TOL["int4"]
+    # the zero row's output is the shared expert and routed experts of x = 0: 0
+    assert np.abs(out[0]).max() == 0.0
