@@ -11,7 +11,7 @@
 // Why 8-bit operands.  With fp16 operand tiles the Int4 GEMM is bound by
 // shared memory: per weight the dequantisers store 2 bytes and the tensor
 // core reads 2 more.  Here the code n - 8 (an integer in [-8, 7], exact in
-// e4m3) is the A operand, 1 byte per weight, and the scale is applied after
+// e5m2) is the A operand, 1 byte per weight, and the scale is applied after
 // the product:
 //   sum_k (n_k - 8) s_g x_k = s_g * sum_{k in g} (n_k - 8) x_k,
 // so each MMA covers exactly one scale group (K = 32 for kind::f8f6f4) into an
@@ -24,17 +24,22 @@
 // exact in fp32, and only fp32 accumulation rounds, as in the fp16 path.
 //
 // B operand: rows 2t (hi) and 2t + 1 (lo) of token t, so N = 16 covers 8
-// tokens; columns past the tile entry's rows are ignored.
+// tokens; columns past the tile entry's rows are ignored.  Along K both
+// operands hold each aligned group of 8 elements in the order
+// (0, 1, 4, 5, 2, 3, 6, 7), the order the weight bytes come out of
+// e5m2_of_codes8.
 //
 // CTA = 15 warps, persistent over the flat tile list:
 //   warp 0, lane 0   code producer: TMA of packed codes, 256 reduction
 //                    elements of both matrices per raw stage
 //   warp 1           TMEM allocation; lane 0 issues tcgen05.mma kind::f8f6f4
+//                    (A e5m2, B e4m3)
 //   warps 2..5       epilogue: per scale group, tcgen05.ld of the group's
 //                    accumulator, scale and add; after the last group the
 //                    clamped SwiGLU and the fp16 h store
 //   warps 6..13      dequantisers, one thread per (weight row, matrix): code
-//                    words -> e4m3 bytes by byte-permute lookups, written
+//                    words -> e5m2 bytes (fp16 mask-and-or, one half2
+//                    subtract, one byte permute per four codes), written
 //                    into the 128-byte-swizzled operand tile
 //   warp 14, lane 0  token producer: TMA of the e4m3 token planes
 // Accumulators: a ring of 8 entries of two groups x (16 gate + 16 up
@@ -103,29 +108,35 @@ __device__ __forceinline__ float clamped_swiglu(float g, float u) {
   return gc / (1.0f + expf(-gc)) * uc;
 }
 
-// Byte permute: bytes 0..3 of a, 4..7 of b, four 4-bit selectors in c[15:0];
-// a selector with bit 3 set gives the selected byte's sign bit replicated.
+// Byte permute: bytes 0..3 of a, 4..7 of b, four 4-bit selectors in c[15:0].
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
-// Four codes (4-bit nibbles in sel[15:0], code j in bits 4j .. 4j+3) ->
-// four e4m3 bytes of code - 8, byte j for code j.  e4m3 of -8 .. -1 is
-// D0 CE CC CA C8 C4 C0 B8, of 0 .. 7 it is 00 38 40 44 48 4A 4C 4E.
-//   a: codes 0..7 look up the negative values; codes 8..15 replicate the
-//      sign of a negative entry: FF.
-//   b: with the selectors' bit 3 flipped, codes 8..15 look up
-//      (value | 80); codes 0..7 replicate a set sign: FF.
-//   a & b is then the value for codes 0..7 and (value | 80) for 8..15;
-//   m (80 in the bytes of codes 8..15) clears that sign.
-__device__ __forceinline__ uint32_t e4m3_of_codes4(uint32_t sel) {
-  const uint32_t a = prmt(0xCACCCED0u, 0xB8C0C4C8u, sel);
-  const uint32_t b = prmt(0xC4C0B880u, 0xCECCCAC8u, sel ^ 0x8888u);
-  const uint32_t s = prmt(sel, 0u, 0x1100u);  // bytes: codes 0,1 | 0,1 | 2,3 | 2,3
-  const uint32_t m = ((s << 4) & 0x00800080u) | (s & 0x80008000u);
-  return (a & b) ^ m;
+// One 32-bit word of codes (code i in bits 4i .. 4i+3) -> eight e5m2 bytes
+// of code - 8, in the operand order (0, 1, 4, 5, 2, 3, 6, 7) of the group
+// of 8.  (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + c0,
+// 1024 + c4) and (w & 0x00F000F0) | 0x54005400 is (64 + c1, 64 + c5);
+// subtracting 1032 (72) leaves c - 8 exactly.  An integer of magnitude <= 8
+// has at most 3 significant bits, so the low byte of its fp16 encoding is
+// zero and the high byte is its e5m2 encoding (same exponent bias, 2
+// mantissa bits): one byte permute packs four of them.
+__device__ __forceinline__ uint2 e5m2_of_codes8(uint32_t w) {
+  const uint32_t w8 = w >> 8;
+  const __half2 lo_off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 hi_off = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));
+  uint32_t q[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                   (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x54005400u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&q[i]), (i & 1) ? hi_off : lo_off);
+    q[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  // q0 = (c0, c4), q1 = (c1, c5), q2 = (c2, c6), q3 = (c3, c7) as fp16 pairs:
+  // high bytes 1 and 3 of each
+  return make_uint2(prmt(q[0], q[1], 0x7351u), prmt(q[2], q[3], 0x7351u));
 }
 
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -313,10 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kGroupsPerSlot; ++j) {
             const uint4 cw = *reinterpret_cast<const uint4*>(ct + (((sb * 4 + j) ^ sw) << 4));
-            const uint4 o0 = make_uint4(e4m3_of_codes4(cw.x), e4m3_of_codes4(cw.x >> 16),
-                                        e4m3_of_codes4(cw.y), e4m3_of_codes4(cw.y >> 16));
-            const uint4 o1 = make_uint4(e4m3_of_codes4(cw.z), e4m3_of_codes4(cw.z >> 16),
-                                        e4m3_of_codes4(cw.w), e4m3_of_codes4(cw.w >> 16));
+            const uint2 e0 = e5m2_of_codes8(cw.x), e1 = e5m2_of_codes8(cw.y);
+            const uint2 e2 = e5m2_of_codes8(cw.z), e3 = e5m2_of_codes8(cw.w);
+            const uint4 o0 = make_uint4(e0.x, e0.y, e1.x, e1.y);
+            const uint4 o1 = make_uint4(e2.x, e2.y, e3.x, e3.y);
             *reinterpret_cast<uint4*>(at + (((2 * j) ^ sw) << 4)) = o0;
             *reinterpret_cast<uint4*>(at + (((2 * j + 1) ^ sw) << 4)) = o1;
           }
@@ -338,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kBM, kBRows, false);  // e4m3 x e4m3, fp32 accumulate
+      // A e5m2 (format 1, bits 7..9), B e4m3 (format 0), fp32 accumulate
+      const uint32_t idesc = idesc_f16(kBM, kBRows, false) | (1u << 7);
       int os = 0, bs = 0, ring = 0;
       uint32_t oph = 0, bph = 0, rph = 0;
       bool ok = true;

@@ -83,8 +83,9 @@ cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_of, int T,
                                 cudaStream_t s);
 // The same copy of each token's row into its k + 1 permuted rows, as two
 // e4m3 planes under a power-of-two scale sigma per token (max |x sigma| in
-// [128, 256)): x8[2r][h] = e4m3(x sigma), x8[2r + 1][h] = e4m3(x sigma -
-// hi), xinv[r] = 1 / sigma.  Also clears zero_n floats of zero_out.
+// [128, 256)): x8[2r][.] = e4m3(x sigma), x8[2r + 1][.] = e4m3(x sigma -
+// hi), each aligned group of 8 columns in the order (0, 1, 4, 5, 2, 3, 6, 7),
+// xinv[r] = 1 / sigma.  Also clears zero_n floats of zero_out.
 cudaError_t launch_split_rows_e4m3(const uint16_t* x, const int32_t* row_of, int T, int H, int k,
                                    uint8_t* x8, float* xinv, float* zero_out, size_t zero_n,
                                    cudaStream_t s);
@@ -175,9 +176,10 @@ struct Int4Launch {
 cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
 
 // Int4 gate/up with the clamped SwiGLU on 8-bit operands (decode sizes):
-// codes n - 8 as e4m3 against the token rows as two e4m3 planes (hi, lo)
-// under a power-of-two scale per row; one MMA per scale group, scales
-// applied by the epilogue.  Tile entries hold at most 8 rows.
+// codes n - 8 as e5m2 against the token rows as two e4m3 planes (hi, lo)
+// under a power-of-two scale per row, each aligned group of 8 elements in
+// the order (0, 1, 4, 5, 2, 3, 6, 7) on both sides; one MMA per scale group,
+// scales applied by the epilogue.  Tile entries hold at most 8 rows.
 constexpr int kF8MaxRows = 8;
 struct Int4F8Launch {
   CUtensorMap tm_c[2];   // codes of the routed gate / up stacks

@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
 // e4m3's range (448).  hi = e4m3(x sigma) and lo = e4m3(x sigma - hi),
 // both rounded to nearest by the hardware conversion; x sigma is exact (a
 // bf16 value times a power of two) and so is x sigma - hi in fp32.  The two
-// planes go to each of the token's k + 1 permuted rows.
+// planes go to each of the token's k + 1 permuted rows, each aligned group
+// of 8 elements in the order (0, 1, 4, 5, 2, 3, 6, 7).
 constexpr int kSplitThreads = 256;
 
 __global__ void __launch_bounds__(kSplitThreads) split_rows_e4m3_kernel(
@@ -266,8 +267,11 @@ __global__ void __launch_bounds__(kSplitThreads) split_rows_e4m3_kernel(
         const __nv_fp8_storage_t h8 = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
         const float hf = __half2float(__half(__nv_cvt_fp8_to_halfraw(h8, __NV_E4M3)));
         const __nv_fp8_storage_t l8 = __nv_cvt_float_to_fp8(y - hf, __NV_SATFINITE, __NV_E4M3);
-        hi[i >> 2] |= static_cast<uint32_t>(h8) << (8 * (i & 3));
-        lo[i >> 2] |= static_cast<uint32_t>(l8) << (8 * (i & 3));
+        // element i goes to byte position (0, 1, 4, 5, 2, 3, 6, 7)[i], the
+        // order in which the 8-bit GEMM's dequantisers emit the weights
+        const int pos = (i & 1) | ((i & 2) << 1) | ((i & 4) >> 1);
+        hi[pos >> 2] |= static_cast<uint32_t>(h8) << (8 * (pos & 3));
+        lo[pos >> 2] |= static_cast<uint32_t>(l8) << (8 * (pos & 3));
       }
       for (int j = 0; j <= k; ++j) {
         uint8_t* rowp = x8 + static_cast<size_t>(s_rows[j]) * 2 * H;
