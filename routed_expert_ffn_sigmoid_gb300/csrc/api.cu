@@ -27,7 +27,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t z, idx, w, blockcnt, offsets, table, table2, gather, row_of, roww, x_perm, xinv, h0, h1,
-      y_perm;
+      hinv, y_perm;
   size_t partial, counters;
   size_t partial_units;  // K-split units the partial buffer holds (0: no split possible)
   size_t total;
@@ -53,10 +53,9 @@ bool int4_f8(const moe_dims& d) { return d.fmt == MOE_W_INT4_G32 && d.T <= 64 &&
 int table_bn(const moe_dims& d) { return int4_f8(d) ? kF8MaxRows : pick_bn(d.T); }
 
 size_t table_bytes(const moe_dims& d) {
-  // every group contributes at most ceil(cnt / 8) entries (entries have at
-  // least 8 rows but the last of a group); the sum is bounded by
-  // (E + 1) + rows / 8
-  const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 7) / 8;
+  // every group contributes at most ceil(cnt / BN) entries with BN >= 5 (the
+  // 8-bit down path's entries), so the sum is bounded by (E + 1) + rows / 4
+  const size_t entries = static_cast<size_t>(d.E + 1) + (rows_of(d) + 3) / 4;
   return kTableHeaderBytes + entries * sizeof(TileEntry);
 }
 
@@ -109,14 +108,15 @@ Layout layout_of(const moe_dims& d) {
   L.blockcnt = take(nblk * E * 4);
   L.offsets = take((E + 2) * 4);
   L.table = take(table_bytes(d));
-  L.table2 = take(int4_f8(d) ? table_bytes(d) : 0);  // down entries of the 8-bit gate/up path
+  L.table2 = take(int4_f8(d) ? table_bytes(d) : 0);  // down entries of the 8-bit path
   L.gather = take(rows * 4);
   L.row_of = take(T * k * 4);
   L.roww = take(rows * 4);
   L.x_perm = take(rows * H * 2);  // Int4 up to 64 tokens: the two e4m3 planes of each row
   L.xinv = take(int4_f8(d) ? rows * 4 : 0);
-  L.h0 = take(rows * I * 2);
+  L.h0 = take(rows * I * (int4_f8(d) ? 3 : 2));  // 8-bit path: three e4m3 planes of h
   L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
+  L.hinv = take(int4_f8(d) ? rows * (I / 32) * 4 : 0);
   L.y_perm = take((d.flags & MOE_FLAG_DETERMINISTIC) ? rows * H * 4 : 0);
   const int tiles = gateup_tiles_bound(d);
   L.partial_units = tiles < kSplitTileLimit ? static_cast<size_t>(tiles) * kMaxSplit : 0;
@@ -245,12 +245,12 @@ bool encode_scales(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// e4m3 token planes of `rows` permuted rows, [2 rows][K] bytes (row 2r: hi,
-// 2r + 1: lo): box {128 bytes, 16 rows}, 128-byte swizzle.
-bool encode_e4m3_planes(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+// e4m3 activation planes, `plane_rows` rows of K bytes (row P r + p: plane p
+// of permuted row r): box {128 bytes, 16 rows}, 128-byte swizzle.
+bool encode_e4m3_planes(CUtensorMap* m, const void* base, uint64_t K, uint64_t plane_rows) {
   const EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {K, 2 * rows};
+  const cuuint64_t dims[2] = {K, plane_rows};
   const cuuint64_t strides[1] = {K};
   const cuuint32_t box[2] = {128, 16};
   const cuuint32_t es[2] = {1, 1};
@@ -387,66 +387,67 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
   const int rows = rows_of(d);
   const int nsm = sm_count();
   if (d.fmt == MOE_W_INT4_G32 && xinv && down_table) {
-    // 8-bit gate/up: x_perm holds the e4m3 planes, entries of <= 8 rows
-    const int max_entries = (d.E + 1) + (rows + kF8MaxRows - 1) / kF8MaxRows;
+    // 8-bit operands: x_perm holds the e4m3 planes of x; gate/up writes h as
+    // three planes, down reads them through its own table
+    uint8_t* h8 = ws.at<uint8_t>(ws.L.h0);
+    float* hinv = ws.at<float>(ws.L.hinv);
     Int4F8Launch G{};
     if (!encode_codes(&G.tm_c[0], ex->gate, d.H, d.I, d.E) ||
         !encode_codes(&G.tm_c[1], ex->up, d.H, d.I, d.E) ||
         !encode_codes(&G.tm_sc[0], sh->gate, d.H, d.I, 1) ||
         !encode_codes(&G.tm_sc[1], sh->up, d.H, d.I, 1) ||
-        !encode_e4m3_planes(&G.tm_b, x_perm, d.H, rows))
+        !encode_e4m3_planes(&G.tm_b, x_perm, d.H, 2 * static_cast<uint64_t>(rows)))
       return MOE_ERR_CUDA;
     G.table = table;
+    G.na = 2;
+    G.epilogue = kEpiStoreRows;
     G.K = d.H;
     G.N_out = d.I;
     G.E = d.E;
     G.total_rows = rows;
-    G.gate_scale = ex->gate_scale;
-    G.up_scale = ex->up_scale;
-    G.sgate_scale = sh->gate_scale;
-    G.sup_scale = sh->up_scale;
-    G.xinv = xinv;
-    G.h = ws.at<void>(ws.L.h0);
+    G.out_rows = d.T;
+    G.scale[0] = ex->gate_scale;
+    G.scale[1] = ex->up_scale;
+    G.sscale[0] = sh->gate_scale;
+    G.sscale[1] = sh->up_scale;
+    G.binv = xinv;
+    G.h8 = h8;
+    G.hinv = hinv;
     G.status = ws.status();
     G.budget_ns = kWaitBudgetNs;
-    const int gtiles = max_entries * (d.I / 128);
+    const int gentries = (d.E + 1) + (rows + kF8MaxRows - 1) / kF8MaxRows;
+    const int gtiles = gentries * (d.I / 128);
     G.grid = gtiles < nsm ? gtiles : nsm;
     record(ev, 2, s);
-    if (launch_int4_f8_gateup(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_int4_f8_gemm(G, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(ev, 3, s);
-    Int4Launch D{};
+    Int4F8Launch D{};
     if (!encode_codes(&D.tm_c[0], ex->down, d.I, d.H, d.E) ||
-        !encode_scales(&D.tm_s[0], ex->down_scale, d.I, d.H, d.E) ||
         !encode_codes(&D.tm_sc[0], sh->down, d.I, d.H, 1) ||
-        !encode_scales(&D.tm_ss[0], sh->down_scale, d.I, d.H, 1) ||
-        !encode_kmajor(&D.tm_b, G.h, false, d.I, rows, 1, 16))
+        !encode_e4m3_planes(&D.tm_b, h8, d.I, 3 * static_cast<uint64_t>(rows)))
       return MOE_ERR_CUDA;
     D.tm_c[1] = D.tm_c[0];
-    D.tm_s[1] = D.tm_s[0];
     D.tm_sc[1] = D.tm_sc[0];
-    D.tm_ss[1] = D.tm_ss[0];
-    // down: its own table, entries of up to pick_bn rows (the shared
-    // expert's rows are not cut into 8-row pieces there)
-    const int dbn = pick_bn(d.T);
-    const int dmax_entries = (d.E + 1) + (rows + dbn - 1) / dbn;
     D.table = down_table;
-    D.BN = dbn;
     D.na = 1;
+    D.epilogue = epilogue;
     D.K = d.I;
     D.N_out = d.H;
-    D.mblocks = d.H / 128;
     D.E = d.E;
     D.total_rows = rows;
     D.out_rows = d.T;
-    D.epilogue = epilogue;
+    D.scale[0] = D.scale[1] = ex->down_scale;
+    D.sscale[0] = D.sscale[1] = sh->down_scale;
+    D.binv = hinv;
     D.gather = gather;
     D.roww = roww;
     D.out = out;
     D.status = ws.status();
     D.budget_ns = kWaitBudgetNs;
-    const int dtiles = dmax_entries * D.mblocks;
+    const int dentries = (d.E + 1) + (rows + kF8DownMaxRows - 1) / kF8DownMaxRows;
+    const int dtiles = dentries * (d.H / 128);
     D.grid = dtiles < nsm ? dtiles : nsm;
-    const cudaError_t e = launch_int4_gemm(D, s);
+    const cudaError_t e = launch_int4_f8_gemm(D, s);
     record(ev, 4, s);
     return from_cuda(e);
   }
@@ -701,7 +702,7 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   // with more threads (measured faster at 64 tokens)
   int32_t* table2 = f8 ? w.at<int32_t>(L.table2) : nullptr;
   const SmallPermOut perm{w.route_done(), table_bn(*d), w.at<int32_t>(L.offsets), gather,
-                          w.at<int32_t>(L.row_of), roww, table, table2, pick_bn(d->T)};
+                          w.at<int32_t>(L.row_of), roww, table, table2, kF8DownMaxRows};
   const bool small = d->T <= kSmallT, fused = d->T <= kFusedPermTokens;
   record(ev, 0, s);
   if ((st = run_router(*d, x, w_router, b_router, idx, wts, w, s, zero_router,

@@ -1,52 +1,57 @@
-// Grouped gate/up GEMM over grouped-Int4 weights on 8-bit tensor-core
-// operands, for decode-size groups (at most 8 tokens per tile entry).
+// Grouped expert GEMMs over grouped-Int4 weights on 8-bit tensor-core
+// operands, for decode-size groups: gate/up with the clamped SwiGLU (NA = 2)
+// and down with the routing weight and the scatter-add (NA = 1).
 //
 // Weights use the grouped fmt=4 Int4 format decoded as offset-binary,
 // value = (nibble - 8) * scale ("feat(glm53): add device-resident HIP backend
 // for MI350P", section "Key changes"), one bf16 scale per 32 reduction
-// elements; gate/up and the clamped SwiGLU follow "Add GLM-5.3-Flash
-// (glm5next) support with ROCmFP mix qtypes (105/106)", section "MoE FFN
-// (REAL routed expert execution)".
+// elements; the expert FFN follows "Add GLM-5.3-Flash (glm5next) support
+// with ROCmFP mix qtypes (105/106)", section "MoE FFN (REAL routed expert
+// execution)".
 //
 // Why 8-bit operands.  With fp16 operand tiles the Int4 GEMM is bound by
 // shared memory: per weight the dequantisers store 2 bytes and the tensor
 // core reads 2 more.  Here the code n - 8 (an integer in [-8, 7], exact in
 // e5m2) is the A operand, 1 byte per weight, and the scale is applied after
 // the product:
-//   sum_k (n_k - 8) s_g x_k = s_g * sum_{k in g} (n_k - 8) x_k,
+//   sum_k (n_k - 8) s_g b_k = s_g * sum_{k in g} (n_k - 8) b_k,
 // so each MMA covers exactly one scale group (K = 32 for kind::f8f6f4) into an
 // accumulator of its own, and the epilogue warps add s_g times it into
-// registers.  The token rows enter as two e4m3 planes under a power-of-two
-// scale per row, hi = e4m3(x sigma) and lo = e4m3(x sigma - hi): bf16 has 8
-// significant bits, hi holds the top 4 and the remainder fits lo's 4, so
-// hi + lo = x sigma exactly except for values more than ~2^-14 below the row
-// maximum (absolute error below 2^-17 of the maximum).  Every product is then
-// exact in fp32, and only fp32 accumulation rounds, as in the fp16 path.
+// registers.  The activation rows (B) enter as e4m3 planes under a power-of-
+// two scale, each plane the rounding remainder of the ones before:
+//   gate/up: x as hi + lo (bf16's 8 significant bits split exactly into
+//            4 + 4), one scale per token row;
+//   down:    h as hi + mid + lo (12 significant bits, one more than fp16),
+//            one scale per token row and group of 32 features, chosen by the
+//            gate/up epilogue from the largest |h| of the group.
+// Every product is exact in fp32; only fp32 accumulation rounds.
 //
-// B operand: rows 2t (hi) and 2t + 1 (lo) of token t, so N = 16 covers 8
-// tokens; columns past the tile entry's rows are ignored.  Along K both
-// operands hold each aligned group of 8 elements in the order
-// (0, 1, 4, 5, 2, 3, 6, 7), the order the weight bytes come out of
-// e5m2_of_codes8.
+// B operand: rows P t .. P t + P - 1 are token t's planes (P = 2 or 3), so
+// N = 16 covers 8 (gate/up) or 5 (down) tokens; columns past the tile
+// entry's rows are ignored.  Along K both operands hold each aligned group of
+// 8 elements in the order (0, 1, 4, 5, 2, 3, 6, 7), the order the weight
+// bytes come out of e5m2_of_codes8.
 //
 // CTA = 15 warps, persistent over the flat tile list:
-//   warp 0, lane 0   code producer: TMA of packed codes, 256 reduction
-//                    elements of both matrices per raw stage
+//   warp 0, lane 0   code producer: TMA of the packed codes, 256 reduction
+//                    elements per raw stage
 //   warp 1           TMEM allocation; lane 0 issues tcgen05.mma kind::f8f6f4
 //                    (A e5m2, B e4m3)
-//   warps 2..5       epilogue: per scale group, tcgen05.ld of the group's
-//                    accumulator, scale and add; after the last group the
-//                    clamped SwiGLU and the fp16 h store
-//   warps 6..13      dequantisers, one thread per (weight row, matrix): code
-//                    words -> e5m2 bytes (fp16 mask-and-or, one half2
-//                    subtract, one byte permute per four codes), written
+//   warps 2..5       epilogue: per two scale groups, tcgen05.ld of their
+//                    accumulators, scale and add; after the last group the
+//                    SwiGLU and the h planes (gate/up) or the scatter-add /
+//                    row store (down)
+//   warps 6..13      dequantisers, two threads per weight row (one per matrix
+//                    for gate/up, one per two of a slot's four groups for
+//                    down): code words -> e5m2 bytes (fp16 mask-and-or, one
+//                    half2 subtract, one byte permute per four codes), written
 //                    into the 128-byte-swizzled operand tile
-//   warp 14, lane 0  token producer: TMA of the e4m3 token planes
-// Accumulators: a ring of 8 entries of two groups x (16 gate + 16 up
-// columns) = 512 TMEM columns; the MMA thread commits and the epilogue warps
-// release one entry per two groups.  Every wait is bounded as in the other
-// GEMM kernels.
+//   warp 14, lane 0  activation producer: TMA of the e4m3 planes
+// Accumulators: a ring of two-group entries over all 512 TMEM columns; the
+// MMA thread commits and the epilogue warps release one entry per two groups.
+// Every wait is bounded as in the other GEMM kernels.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "moe_kernels.h"
 #include "ptx.cuh"
@@ -55,43 +60,54 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kSlotK = 128;                        // e4m3 per 128-byte swizzle row
+constexpr int kSlotK = 128;                        // 8-bit elements per 128-byte swizzle row
 constexpr int kRawK = 256;                         // reduction elements per raw stage
 constexpr int kSlotsPerRaw = kRawK / kSlotK;       // 2
 constexpr int kGroupsPerSlot = kSlotK / 32;        // 4
-constexpr int kATileBytes = kBM * kSlotK;          // 16 KB e4m3 operand per matrix
-constexpr int kSlotBytes = 2 * kATileBytes;        // gate + up
+constexpr int kATileBytes = kBM * kSlotK;          // 16 KB e5m2 operand per matrix
 constexpr int kCodeTileBytes = kBM * (kRawK / 2);  // 16 KB packed codes per matrix
-constexpr int kRawBytes = 2 * kCodeTileBytes;
-constexpr int kBRows = 16;                         // hi/lo rows of up to 8 tokens
+constexpr int kBRows = 16;
 constexpr int kBTileBytes = kBRows * kSlotK;       // 2 KB
-constexpr int kRaw = 4;
-constexpr int kSlots = 2;
 constexpr int kBStages = 8;
 constexpr int kGroupsPerSync = 2;                  // groups per accumulator handshake
-constexpr int kAccRing = 8;                        // handshakes in flight (16 groups)
-constexpr int kAccCols = 32 * kGroupsPerSync;      // per group: 16 gate + 16 up columns
-constexpr int kTmemCols = kAccRing * kAccCols;     // 512
+constexpr int kTmemCols = 512;
 constexpr int kBarBytes = 1024;
-constexpr int kSmemBytes =
-    kSlots * kSlotBytes + kRaw * kRawBytes + kBStages * kBTileBytes + 1024 + kBarBytes;
 constexpr int kThreads = 480;
 constexpr int kDqThread0 = 192;
 constexpr int kDqThreads = 256;
 constexpr int kDqWarpEnd = 14;
 constexpr int kBWarp = 14;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(kTmemCols == 512, "TMEM");
+
+template <int NA>
+struct F8Cfg {
+  static constexpr int kPlanes = NA == 2 ? 2 : 3;             // B rows per token
+  static constexpr int kMaxTok = kBRows / kPlanes;            // 8 or 5
+  static constexpr int kGroupCols = 16 * NA;                  // accumulator columns per group
+  static constexpr int kEntryCols = kGroupsPerSync * kGroupCols;
+  static constexpr int kAccRing = kTmemCols / kEntryCols;     // 8 or 16
+  static constexpr int kSlotBytes = NA * kATileBytes;
+  static constexpr int kRawBytes = NA * kCodeTileBytes;
+  static constexpr int kRaw = NA == 2 ? 4 : 6;
+  static constexpr int kSlots = NA == 2 ? 2 : 3;
+  static constexpr int kSmemBytes =
+      kSlots * kSlotBytes + kRaw * kRawBytes + kBStages * kBTileBytes + 1024 + kBarBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kMaxTok == (NA == 2 ? kF8MaxRows : kF8DownMaxRows), "tile entry rows");
+};
 
 struct F8Args {
   const int32_t* table;
-  int K, N_out, mblocks, E, total_rows;
-  const uint16_t* gate_scale;   // routed scales [E][N_out][K / 32] bf16
-  const uint16_t* up_scale;
-  const uint16_t* sgate_scale;  // shared expert [1][N_out][K / 32]
-  const uint16_t* sup_scale;
-  const float* xinv;            // per token row: 1 / sigma
-  __half* h;                    // [rows][N_out], columns in the Int4 operand order
+  int K, N_out, mblocks, E, total_rows, out_rows;
+  const uint16_t* scale0;   // routed scales [E][N_out][K / 32] bf16 (gate, or down)
+  const uint16_t* scale1;   // (up)
+  const uint16_t* sscale0;  // shared expert [1][N_out][K / 32]
+  const uint16_t* sscale1;
+  const float* binv;        // gate/up: [rows] 1 / sigma; down: [rows][K / 32]
+  uint8_t* h8;              // gate/up: h planes [rows][3][N_out]
+  float* hinv;              // gate/up: [rows][N_out / 32]
+  const int32_t* gather;    // down
+  const float* roww;
+  float* out;               // down: scatter-add [T][N_out] or rows [rows][N_out]
   int* status;
   uint64_t budget_ns;
 };
@@ -139,6 +155,9 @@ __device__ __forceinline__ uint2 e5m2_of_codes8(uint32_t w) {
   return make_uint2(prmt(q[0], q[1], 0x7351u), prmt(q[2], q[3], 0x7351u));
 }
 
+// Position of element i (0..7) of an aligned group of 8 in that order.
+__device__ __forceinline__ int op_pos8(int i) { return (i & 1) | ((i & 2) << 1) | ((i & 4) >> 1); }
+
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -168,33 +187,69 @@ __device__ __forceinline__ float scale_of(const uint4& v, int g) {
   return (g & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
+// 4 x 4 transpose across the four lanes 4j .. 4j+3 of a warp: lane 4j+r
+// holds row r, (x0, x1, x2, x3) = M[r][0..3], and ends with column r.
+__device__ __forceinline__ void transpose4_lanes(float& x0, float& x1, float& x2, float& x3,
+                                                 int lane) {
+  const bool o1 = lane & 1, o2 = lane & 2;
+  float s0 = __shfl_xor_sync(0xffffffffu, o1 ? x0 : x1, 1);
+  float s1 = __shfl_xor_sync(0xffffffffu, o1 ? x2 : x3, 1);
+  if (o1) {
+    x0 = s0;
+    x2 = s1;
+  } else {
+    x1 = s0;
+    x3 = s1;
+  }
+  s0 = __shfl_xor_sync(0xffffffffu, o2 ? x0 : x2, 2);
+  s1 = __shfl_xor_sync(0xffffffffu, o2 ? x1 : x3, 2);
+  if (o2) {
+    x0 = s0;
+    x1 = s1;
+  } else {
+    x2 = s0;
+    x3 = s1;
+  }
+}
+
+__device__ __forceinline__ uint8_t e4m3_rn(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_value(uint8_t b) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(b, __NV_E4M3)));
+}
+
+template <int NA, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    int4_f8_gateup_kernel(const __grid_constant__ CUtensorMap tm_c0,
-                          const __grid_constant__ CUtensorMap tm_c1,
-                          const __grid_constant__ CUtensorMap tm_sc0,
-                          const __grid_constant__ CUtensorMap tm_sc1,
-                          const __grid_constant__ CUtensorMap tm_b, const F8Args a) {
+    int4_f8_gemm_kernel(const __grid_constant__ CUtensorMap tm_c0,
+                        const __grid_constant__ CUtensorMap tm_c1,
+                        const __grid_constant__ CUtensorMap tm_sc0,
+                        const __grid_constant__ CUtensorMap tm_sc1,
+                        const __grid_constant__ CUtensorMap tm_b, const F8Args a) {
+  using Cfg = F8Cfg<NA>;
+  constexpr int P = Cfg::kPlanes;
+  constexpr int kTok = Cfg::kMaxTok;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* slots = base;
-  uint8_t* raws = slots + kSlots * kSlotBytes;
-  uint8_t* bring = raws + kRaw * kRawBytes;
+  uint8_t* raws = slots + Cfg::kSlots * Cfg::kSlotBytes;
+  uint8_t* bring = raws + Cfg::kRaw * Cfg::kRawBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bring + kBStages * kBTileBytes);
   uint64_t* raw_full = bars;
-  uint64_t* raw_empty = raw_full + kRaw;
-  uint64_t* b_full = raw_empty + kRaw;
+  uint64_t* raw_empty = raw_full + Cfg::kRaw;
+  uint64_t* b_full = raw_empty + Cfg::kRaw;
   uint64_t* b_empty = b_full + kBStages;
   uint64_t* a_full = b_empty + kBStages;
-  uint64_t* op_empty = a_full + kSlots;
-  uint64_t* acc_full = op_empty + kSlots;
-  uint64_t* acc_empty = acc_full + kAccRing;
-  uint64_t* drain = acc_empty + kAccRing;
+  uint64_t* op_empty = a_full + Cfg::kSlots;
+  uint64_t* acc_full = op_empty + Cfg::kSlots;
+  uint64_t* acc_empty = acc_full + Cfg::kAccRing;
+  uint64_t* drain = acc_empty + Cfg::kAccRing;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRaw; ++i) {
+    for (int i = 0; i < Cfg::kRaw; ++i) {
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kDqThreads);
     }
@@ -202,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < Cfg::kSlots; ++i) {
       mbar_init(&a_full[i], kDqThreads);
       mbar_init(&op_empty[i], 1);
     }
-    for (int i = 0; i < kAccRing; ++i) {
+    for (int i = 0; i < Cfg::kAccRing; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 128);
     }
@@ -231,8 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KS = a.K / kSlotK;     // operand slots per tile
   const int G = a.K / 32;          // scale groups per tile
 
-  auto code_tile = [&](int rs, int m) { return raws + rs * kRawBytes + m * kCodeTileBytes; };
-  auto a_tile = [&](int os, int m) { return slots + os * kSlotBytes + m * kATileBytes; };
+  auto code_tile = [&](int rs, int m) {
+    return raws + rs * Cfg::kRawBytes + m * kCodeTileBytes;
+  };
+  auto a_tile = [&](int os, int m) { return slots + os * Cfg::kSlotBytes + m * kATileBytes; };
   auto b_tile = [&](int bs) { return bring + bs * kBTileBytes; };
 
   if (warp == 0) {
@@ -252,24 +309,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
+          mbar_arrive_expect_tx(&raw_full[rs], Cfg::kRawBytes);
           armed |= 1u << rs;
           armed_par = (armed_par & ~(1u << rs)) | (rph << rs);
           tma_load_3d(code_tile(rs, 0), sh ? &tm_sc0 : &tm_c0, &raw_full[rs], rb * (kRawK / 2),
                       mb * kBM, ge, pol);
-          tma_load_3d(code_tile(rs, 1), sh ? &tm_sc1 : &tm_c1, &raw_full[rs], rb * (kRawK / 2),
-                      mb * kBM, ge, pol);
-          if (++rs == kRaw) {
+          if (NA == 2)
+            tma_load_3d(code_tile(rs, 1), sh ? &tm_sc1 : &tm_c1, &raw_full[rs], rb * (kRawK / 2),
+                        mb * kBM, ge, pol);
+          if (++rs == Cfg::kRaw) {
             rs = 0;
             rph ^= 1u;
           }
         }
       }
-      for (int s = 0; s < kRaw; ++s)
+      for (int s = 0; s < Cfg::kRaw; ++s)
         if ((armed >> s) & 1u) mbar_wait_drain(&raw_full[s], (armed_par >> s) & 1u);
     }
   } else if (warp == kBWarp) {
-    // ---------------------------------------------------------------- token producer
+    // ---------------------------------------------------------------- activation producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       int bs = 0;
@@ -285,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&b_full[bs], kBTileBytes);
           armed |= 1u << bs;
           armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
-          tma_load_2d(b_tile(bs), &tm_b, &b_full[bs], ks * kSlotK, 2 * te.row0, pol);
+          tma_load_2d(b_tile(bs), &tm_b, &b_full[bs], ks * kSlotK, P * te.row0, pol);
           if (++bs == kBStages) {
             bs = 0;
             bph ^= 1u;
@@ -298,9 +356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 6 && warp < kDqWarpEnd) {
     // ---------------------------------------------------------------- dequantisers
     const int d = threadIdx.x - kDqThread0;
-    const int r = d & (kBM - 1);  // weight row of the tile
-    const int m = d >> 7;         // matrix: 0 gate, 1 up
-    const int sw = r & 7;         // 128-byte swizzle phase of this row
+    const int r = d & (kBM - 1);                // weight row of the tile
+    const int m = NA == 2 ? (d >> 7) : 0;       // gate/up: matrix
+    const int j0 = NA == 2 ? 0 : (d >> 7) * 2;  // down: first of two groups per slot
+    constexpr int kJ = NA == 2 ? kGroupsPerSlot : 2;
+    const int sw = r & 7;                       // 128-byte swizzle phase of this row
     int rs = 0, os = 0;
     uint32_t rph = 0, oph = 0;
     bool ok = true;
@@ -318,29 +378,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* at = a_tile(os, m) + r * 128;
-          // 128 codes of this slot: code chunks 4 sb .. 4 sb + 3 (32 codes,
-          // one scale group each) -> e4m3 chunks 8 j' .. : chunk 2 j (+1)
-          // holds codes 32 j .. 32 j + 15 (+16).
+          // code chunk 4 sb + j (32 codes, one scale group) -> operand chunks
+          // 2 j and 2 j + 1 (16 codes each)
 #pragma unroll
-          for (int j = 0; j < kGroupsPerSlot; ++j) {
+          for (int jj = 0; jj < kJ; ++jj) {
+            const int j = j0 + jj;
             const uint4 cw = *reinterpret_cast<const uint4*>(ct + (((sb * 4 + j) ^ sw) << 4));
             const uint2 e0 = e5m2_of_codes8(cw.x), e1 = e5m2_of_codes8(cw.y);
             const uint2 e2 = e5m2_of_codes8(cw.z), e3 = e5m2_of_codes8(cw.w);
-            const uint4 o0 = make_uint4(e0.x, e0.y, e1.x, e1.y);
-            const uint4 o1 = make_uint4(e2.x, e2.y, e3.x, e3.y);
-            *reinterpret_cast<uint4*>(at + (((2 * j) ^ sw) << 4)) = o0;
-            *reinterpret_cast<uint4*>(at + (((2 * j + 1) ^ sw) << 4)) = o1;
+            *reinterpret_cast<uint4*>(at + (((2 * j) ^ sw) << 4)) =
+                make_uint4(e0.x, e0.y, e1.x, e1.y);
+            *reinterpret_cast<uint4*>(at + (((2 * j + 1) ^ sw) << 4)) =
+                make_uint4(e2.x, e2.y, e3.x, e3.y);
           }
           fence_proxy_async_smem();
           mbar_arrive(&a_full[os]);
-          if (++os == kSlots) {
+          if (++os == Cfg::kSlots) {
             os = 0;
             oph ^= 1u;
           }
         }
         if (!ok) break;
         mbar_arrive(&raw_empty[rs]);
-        if (++rs == kRaw) {
+        if (++rs == Cfg::kRaw) {
           rs = 0;
           rph ^= 1u;
         }
@@ -362,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(bs)));
-          const uint64_t dg = sw128_kmajor_desc(smem_u32(a_tile(os, 0)));
-          const uint64_t du = sw128_kmajor_desc(smem_u32(a_tile(os, 1)));
+          const uint64_t d0 = sw128_kmajor_desc(smem_u32(a_tile(os, 0)));
+          const uint64_t d1 = sw128_kmajor_desc(smem_u32(a_tile(os, NA - 1)));
 #pragma unroll
           for (int j0 = 0; j0 < kGroupsPerSlot; j0 += kGroupsPerSync) {
             if (!mbar_wait(&acc_empty[ring], rph ^ 1u, ab)) {
@@ -374,12 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < kGroupsPerSync; ++jj) {
               const int j = j0 + jj;
-              const uint32_t dacc = tmem_base + ring * kAccCols + jj * 32;
-              umma_f8(dacc, dg + 2 * j, db + 2 * j, idesc, 0u);
-              umma_f8(dacc + 16, du + 2 * j, db + 2 * j, idesc, 0u);
+              const uint32_t dacc = tmem_base + ring * Cfg::kEntryCols + jj * Cfg::kGroupCols;
+              umma_f8(dacc, d0 + 2 * j, db + 2 * j, idesc, 0u);
+              if (NA == 2) umma_f8(dacc + 16, d1 + 2 * j, db + 2 * j, idesc, 0u);
             }
             umma_commit(&acc_full[ring]);
-            if (++ring == kAccRing) {
+            if (++ring == Cfg::kAccRing) {
               ring = 0;
               rph ^= 1u;
             }
@@ -387,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           umma_commit(&op_empty[os]);
           umma_commit(&b_empty[bs]);
-          if (++os == kSlots) {
+          if (++os == Cfg::kSlots) {
             os = 0;
             oph ^= 1u;
           }
@@ -411,19 +471,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileEntry te = entry_at(a.table, tile / a.mblocks);
       const int mb = tile % a.mblocks;
       const bool sh = te.group == a.E;
-      const int f = mb * kBM + r;  // feature (N_out % 128 == 0)
+      const int f = mb * kBM + r;  // output feature (N_out % 128 == 0)
+      const int nt = min(te.nrows, kTok);
       const size_t srow = (static_cast<size_t>(sh ? 0 : te.group) * a.N_out + f) * G;
-      const uint4* sgp = reinterpret_cast<const uint4*>((sh ? a.sgate_scale : a.gate_scale) + srow);
-      const uint4* sup = reinterpret_cast<const uint4*>((sh ? a.sup_scale : a.up_scale) + srow);
-      const int live = 2 * te.nrows;  // accumulator columns that hold tokens
-      float ag[16], au[16];
+      const uint4* s0p = reinterpret_cast<const uint4*>((sh ? a.sscale0 : a.scale0) + srow);
+      const uint4* s1p = reinterpret_cast<const uint4*>((sh ? a.sscale1 : a.scale1) + srow);
+      // down, scatter-add: lane l < nt holds token l's id and routing weight
+      int tk = -1;
+      float tw = 0.f;
+      if (NA == 1 && EPI == kEpiScatterAdd && lane < nt && te.row0 + lane < a.total_rows) {
+        const int t = a.gather[te.row0 + lane];
+        tw = a.roww[te.row0 + lane];
+        tk = (t >= 0 && t < a.out_rows) ? t : -1;
+      }
+      // gate/up: (gate, up) per B column; down: per token
+      float acc0[NA == 2 ? 16 : kTok], acc1[NA == 2 ? 16 : 1];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) ag[c] = au[c] = 0.f;
-      uint4 sg = __ldg(sgp), su = __ldg(sup);
+      for (int c = 0; c < (NA == 2 ? 16 : kTok); ++c) acc0[c] = 0.f;
+#pragma unroll
+      for (int c = 0; c < (NA == 2 ? 16 : 1); ++c) acc1[c] = 0.f;
+      uint4 s0 = __ldg(s0p), s1 = NA == 2 ? __ldg(s1p) : s0;
       for (int g8 = 0; ok && g8 < G; g8 += 8) {
         // the next eight scales of each matrix, loaded one batch ahead
-        const uint4 sgn = g8 + 8 < G ? __ldg(sgp + g8 / 8 + 1) : sg;
-        const uint4 sun = g8 + 8 < G ? __ldg(sup + g8 / 8 + 1) : su;
+        const uint4 s0n = g8 + 8 < G ? __ldg(s0p + g8 / 8 + 1) : s0;
+        const uint4 s1n = (NA == 2 && g8 + 8 < G) ? __ldg(s1p + g8 / 8 + 1) : s1;
+        // down: each token's h scales (1 / sigma) of these eight groups
+        float hb[NA == 1 ? kTok : 1][8];
+        if (NA == 1) {
+#pragma unroll
+          for (int t = 0; t < (NA == 1 ? kTok : 1); ++t) {
+            const int rr = te.row0 + t;
+            if (t < nt && rr < a.total_rows) {
+              const float4* hp =
+                  reinterpret_cast<const float4*>(a.binv + static_cast<size_t>(rr) * G + g8);
+              const float4 v0 = __ldg(hp), v1 = __ldg(hp + 1);
+              hb[t][0] = v0.x;
+              hb[t][1] = v0.y;
+              hb[t][2] = v0.z;
+              hb[t][3] = v0.w;
+              hb[t][4] = v1.x;
+              hb[t][5] = v1.y;
+              hb[t][6] = v1.z;
+              hb[t][7] = v1.w;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hb[t][i] = 0.f;
+            }
+          }
+        }
 #pragma unroll
         for (int gi = 0; gi < 8; gi += kGroupsPerSync) {
           if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ring], rph, ab))) {
@@ -431,66 +526,131 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ring * kAccCols;
-          if (live <= 8) {
-            // at most 4 tokens: columns 0..7 of each accumulator
-            uint32_t v[kGroupsPerSync][2][8];
+          const uint32_t tq =
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ring * Cfg::kEntryCols;
+          if (NA == 2) {
+            if (2 * nt <= 8) {  // at most 4 tokens: columns 0..7 of each accumulator
+              uint32_t v[kGroupsPerSync][2][8];
 #pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              tmem_ld_32x32b_x8(tq + jj * 32, v[jj][0]);
-              tmem_ld_32x32b_x8(tq + jj * 32 + 16, v[jj][1]);
-            }
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&acc_empty[ring]);
+              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
+                tmem_ld_32x32b_x8(tq + jj * 32, v[jj][0]);
+                tmem_ld_32x32b_x8(tq + jj * 32 + 16, v[jj][1]);
+              }
+              tmem_ld_wait();
+              tc_fence_before_sync();
+              mbar_arrive(&acc_empty[ring]);
 #pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              const float s_g = scale_of(sg, gi + jj), s_u = scale_of(su, gi + jj);
+              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
+                const float sa = scale_of(s0, gi + jj), sb = scale_of(s1, gi + jj);
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                ag[c] = fmaf(s_g, __uint_as_float(v[jj][0][c]), ag[c]);
-                au[c] = fmaf(s_u, __uint_as_float(v[jj][1][c]), au[c]);
+                for (int c = 0; c < 8; ++c) {
+                  acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
+                  acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                }
+              }
+            } else {
+              uint32_t v[kGroupsPerSync][2][16];
+#pragma unroll
+              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
+                tmem_ld_32x32b_x16(tq + jj * 32, v[jj][0]);
+                tmem_ld_32x32b_x16(tq + jj * 32 + 16, v[jj][1]);
+              }
+              tmem_ld_wait();
+              tc_fence_before_sync();
+              mbar_arrive(&acc_empty[ring]);
+#pragma unroll
+              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
+                const float sa = scale_of(s0, gi + jj), sb = scale_of(s1, gi + jj);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
+                  acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                }
               }
             }
           } else {
-            uint32_t v[kGroupsPerSync][2][16];
+            uint32_t v[kGroupsPerSync][16];
 #pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              tmem_ld_32x32b_x16(tq + jj * 32, v[jj][0]);
-              tmem_ld_32x32b_x16(tq + jj * 32 + 16, v[jj][1]);
-            }
+            for (int jj = 0; jj < kGroupsPerSync; ++jj) tmem_ld_32x32b_x16(tq + jj * 16, v[jj]);
             tmem_ld_wait();
             tc_fence_before_sync();
             mbar_arrive(&acc_empty[ring]);
 #pragma unroll
             for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              const float s_g = scale_of(sg, gi + jj), s_u = scale_of(su, gi + jj);
+              const float sa = scale_of(s0, gi + jj);
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                ag[c] = fmaf(s_g, __uint_as_float(v[jj][0][c]), ag[c]);
-                au[c] = fmaf(s_u, __uint_as_float(v[jj][1][c]), au[c]);
+              for (int t = 0; t < kTok; ++t) {
+                const float pv = (__uint_as_float(v[jj][3 * t]) +
+                                  __uint_as_float(v[jj][3 * t + 1])) +
+                                 __uint_as_float(v[jj][3 * t + 2]);
+                acc0[t] = fmaf(sa * hb[NA == 1 ? t : 0][gi + jj], pv, acc0[t]);
               }
             }
           }
-          if (++ring == kAccRing) {
+          if (++ring == Cfg::kAccRing) {
             ring = 0;
             rph ^= 1u;
           }
         }
-        sg = sgn;
-        su = sun;
+        s0 = s0n;
+        s1 = s1n;
       }
       if (!ok) break;
-      // column of feature f in the down GEMM's operand order (see expert_gemm_int4.cu)
-      const int f_op = (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1);
+      if (NA == 2) {
+        // SwiGLU, then h as three e4m3 planes under a power-of-two scale per
+        // (token, group of 32 features): the warp's 32 lanes are one group
+        const int g32 = f >> 5;
+        const int fpos = (f & ~7) | op_pos8(f & 7);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int rr = te.row0 + t;
-        if (t < te.nrows && rr < a.total_rows) {
-          const float inv = __ldg(a.xinv + rr);
-          const float gv = (ag[2 * t] + ag[2 * t + 1]) * inv;
-          const float uv = (au[2 * t] + au[2 * t + 1]) * inv;
-          a.h[static_cast<size_t>(rr) * a.N_out + f_op] = __float2half_rn(clamped_swiglu(gv, uv));
+        for (int t = 0; t < kTok; ++t) {
+          const int rr = te.row0 + t;
+          if (t < nt && rr < a.total_rows) {  // the same for the whole warp
+            const float inv = __ldg(a.binv + rr);
+            const float gv = (acc0[2 * t] + acc0[2 * t + 1]) * inv;
+            const float uv = (acc1[2 * t] + acc1[2 * t + 1]) * inv;
+            const float hv = clamped_swiglu(gv, uv);
+            float mx = fabsf(hv);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            int e = 0;
+            if (mx > 0.f) frexpf(mx, &e);
+            e = max(e, -100);
+            const float sigma = ldexpf(1.0f, 8 - e);  // max |h sigma| in [128, 256)
+            const float y = hv * sigma;
+            const uint8_t b0 = e4m3_rn(y);
+            const float r1 = y - e4m3_value(b0);
+            const uint8_t b1 = e4m3_rn(r1);
+            const uint8_t b2 = e4m3_rn(r1 - e4m3_value(b1));
+            uint8_t* hp = a.h8 + static_cast<size_t>(rr) * 3 * a.N_out + fpos;
+            hp[0] = b0;
+            hp[a.N_out] = b1;
+            hp[2 * a.N_out] = b2;
+            if (lane == 0) a.hinv[static_cast<size_t>(rr) * (a.N_out / 32) + g32] = 1.0f / sigma;
+          }
+        }
+      } else if (EPI == kEpiScatterAdd) {
+        // lanes 4j .. 4j+3 hold four consecutive features: a 4 x 4 exchange
+        // gives lane 4j+r those features of token tg + r, one 16-byte atomic
+        const int r4 = lane & 3;
+        float* const ob = a.out + (f & ~3);
+#pragma unroll
+        for (int tg = 0; tg < kTok; tg += 4) {
+          float x[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[i] = tg + i < kTok ? acc0[(tg + i) % kTok] : 0.f;
+          transpose4_lanes(x[0], x[1], x[2], x[3], lane);
+          const int t = tg + r4;
+          const int tok = __shfl_sync(0xffffffffu, tk, t & 31);
+          const float wr = __shfl_sync(0xffffffffu, tw, t & 31);
+          if (t < nt && tok >= 0)
+            atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(tok) * a.N_out),
+                      make_float4(wr * x[0], wr * x[1], wr * x[2], wr * x[3]));
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+          const int rr = te.row0 + t;
+          if (t < nt && rr < a.total_rows) a.out[static_cast<size_t>(rr) * a.N_out + f] = acc0[t];
         }
       }
     }
@@ -502,22 +662,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_int4_f8_gateup(const Int4F8Launch& L, cudaStream_t s) {
-  if (L.K % kRawK != 0 || L.N_out % kBM != 0) return cudaErrorInvalidValue;
-  auto kern = int4_f8_gateup_kernel;
+template <int NA, int EPI>
+cudaError_t f8_dispatch(const Int4F8Launch& L, cudaStream_t s) {
+  using Cfg = F8Cfg<NA>;
+  auto kern = int4_f8_gemm_kernel<NA, EPI>;
   cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  F8Args a{L.table, L.K, L.N_out, L.N_out / kBM, L.E, L.total_rows,
-           static_cast<const uint16_t*>(L.gate_scale), static_cast<const uint16_t*>(L.up_scale),
-           static_cast<const uint16_t*>(L.sgate_scale), static_cast<const uint16_t*>(L.sup_scale),
-           L.xinv, static_cast<__half*>(L.h), L.status, L.budget_ns};
+  F8Args a{L.table, L.K, L.N_out, L.N_out / kBM, L.E, L.total_rows, L.out_rows,
+           static_cast<const uint16_t*>(L.scale[0]), static_cast<const uint16_t*>(L.scale[1]),
+           static_cast<const uint16_t*>(L.sscale[0]), static_cast<const uint16_t*>(L.sscale[1]),
+           L.binv, L.h8, L.hinv, L.gather, L.roww, L.out, L.status, L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -525,6 +684,15 @@ cudaError_t launch_int4_f8_gateup(const Int4F8Launch& L, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, L.tm_c[0], L.tm_c[1], L.tm_sc[0], L.tm_sc[1], L.tm_b, a);
+}
+
+}  // namespace
+
+cudaError_t launch_int4_f8_gemm(const Int4F8Launch& L, cudaStream_t s) {
+  if (L.K % kRawK != 0 || L.N_out % kBM != 0) return cudaErrorInvalidValue;
+  if (L.na == 2) return f8_dispatch<2, kEpiStoreRows>(L, s);
+  if (L.epilogue == kEpiScatterAdd) return f8_dispatch<1, kEpiScatterAdd>(L, s);
+  return f8_dispatch<1, kEpiStoreRows>(L, s);
 }
 
 }  // namespace moe

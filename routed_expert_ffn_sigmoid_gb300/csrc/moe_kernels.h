@@ -175,29 +175,37 @@ struct Int4Launch {
 };
 cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
 
-// Int4 gate/up with the clamped SwiGLU on 8-bit operands (decode sizes):
-// codes n - 8 as e5m2 against the token rows as two e4m3 planes (hi, lo)
-// under a power-of-two scale per row, each aligned group of 8 elements in
-// the order (0, 1, 4, 5, 2, 3, 6, 7) on both sides; one MMA per scale group,
-// scales applied by the epilogue.  Tile entries hold at most 8 rows.
+// Int4 grouped GEMMs on 8-bit operands (decode sizes): codes n - 8 as e5m2
+// against the activation rows as e4m3 planes under power-of-two scales, each
+// aligned group of 8 elements in the order (0, 1, 4, 5, 2, 3, 6, 7) on both
+// sides; one MMA per scale group, scales applied by the epilogue.
+//   na = 2: gate/up with the clamped SwiGLU.  B: x as two planes (hi, lo),
+//           binv [rows] = 1 / sigma; tile entries of at most kF8MaxRows rows.
+//           Writes h as three planes h8 [rows][3][N_out] (hi, mid, lo) and
+//           hinv [rows][N_out / 32] = 1 / sigma per group of 32 features.
+//   na = 1: down with the scatter-add or store-rows epilogue.  B: those h
+//           planes, binv = hinv; tile entries of at most kF8DownMaxRows rows.
 constexpr int kF8MaxRows = 8;
+constexpr int kF8DownMaxRows = 5;
 struct Int4F8Launch {
-  CUtensorMap tm_c[2];   // codes of the routed gate / up stacks
-  CUtensorMap tm_sc[2];  // codes of the shared expert's gate / up
-  CUtensorMap tm_b;      // e4m3 token planes: [2 rows][K] bytes, row 2r hi, 2r + 1 lo
+  CUtensorMap tm_c[2];   // codes of the routed stacks (gate, up; or down)
+  CUtensorMap tm_sc[2];  // codes of the shared expert
+  CUtensorMap tm_b;      // e4m3 activation planes, row P r + p
   const int32_t* table;
-  int K, N_out, E, total_rows;
-  const void* gate_scale;   // bf16 [E][N_out][K / 32]
-  const void* up_scale;
-  const void* sgate_scale;  // bf16 [1][N_out][K / 32]
-  const void* sup_scale;
-  const float* xinv;        // [rows] 1 / sigma of each token row
-  void* h;                  // fp16 [rows][N_out] in the Int4 operand order
+  int na, epilogue, K, N_out, E, total_rows, out_rows;
+  const void* scale[2];   // bf16 [E][N_out][K / 32]
+  const void* sscale[2];  // bf16 [1][N_out][K / 32]
+  const float* binv;
+  uint8_t* h8;
+  float* hinv;
+  const int32_t* gather;
+  const float* roww;
+  float* out;
   int* status;
   uint64_t budget_ns;
   int grid;
 };
-cudaError_t launch_int4_f8_gateup(const Int4F8Launch& L, cudaStream_t s);
+cudaError_t launch_int4_f8_gemm(const Int4F8Launch& L, cudaStream_t s);
 
 // Token-major grouped GEMM (bf16, token tiles of 128 rows): gate/up with the
 // SwiGLU epilogue (h hi/lo planes) or down with the scatter-add / store-rows
