@@ -47,7 +47,9 @@ int pick_bn(int T) {
 
 // Int4 weights up to 64 tokens: gate/up on 8-bit operands (entries of at
 // most kF8MaxRows rows), down on the fp16 path over the same entries.
-bool int4_f8(const moe_dims& d) { return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0; }
+bool int4_f8(const moe_dims& d) {
+  return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0 && d.I <= 4096;
+}
 
 // Rows per tile-table entry of the fused layer.
 int table_bn(const moe_dims& d) { return int4_f8(d) ? kF8MaxRows : pick_bn(d.T); }

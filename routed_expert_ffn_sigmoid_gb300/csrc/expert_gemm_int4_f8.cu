@@ -77,6 +77,7 @@ constexpr int kDqThread0 = 192;
 constexpr int kDqThreads = 256;
 constexpr int kDqWarpEnd = 14;
 constexpr int kBWarp = 14;
+constexpr int kMaxGroups = 128;                    // K / 32 of the down projection (I <= 4096)
 
 template <int NA>
 struct F8Cfg {
@@ -230,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int P = Cfg::kPlanes;
   constexpr int kTok = Cfg::kMaxTok;
   extern __shared__ uint8_t smem_raw[];
+  // down: each epilogue warp's copy of its tile's h scales [token][group]
+  __shared__ float s_hb[NA == 1 ? 4 : 1][NA == 1 ? kTok : 1][NA == 1 ? kMaxGroups : 1];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* slots = base;
   uint8_t* raws = slots + Cfg::kSlots * Cfg::kSlotBytes;
@@ -490,35 +493,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < (NA == 2 ? 16 : kTok); ++c) acc0[c] = 0.f;
 #pragma unroll
       for (int c = 0; c < (NA == 2 ? 16 : 1); ++c) acc1[c] = 0.f;
+      if (NA == 1) {
+        // the tile's h scales (1 / sigma) for every token and group, loaded
+        // once into this warp's shared-memory copy (the warp's previous tile
+        // is done with it: all lanes passed its group loop)
+        __syncwarp();
+        for (int i = lane; i < kTok * G; i += 32) {
+          const int t = i / G, g = i - t * G;
+          const int rr = te.row0 + t;
+          s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g : 0] =
+              (t < nt && rr < a.total_rows) ? __ldg(a.binv + static_cast<size_t>(rr) * G + g) : 0.f;
+        }
+        __syncwarp();
+      }
       uint4 s0 = __ldg(s0p), s1 = NA == 2 ? __ldg(s1p) : s0;
       for (int g8 = 0; ok && g8 < G; g8 += 8) {
         // the next eight scales of each matrix, loaded one batch ahead
         const uint4 s0n = g8 + 8 < G ? __ldg(s0p + g8 / 8 + 1) : s0;
         const uint4 s1n = (NA == 2 && g8 + 8 < G) ? __ldg(s1p + g8 / 8 + 1) : s1;
-        // down: each token's h scales (1 / sigma) of these eight groups
-        float hb[NA == 1 ? kTok : 1][8];
-        if (NA == 1) {
-#pragma unroll
-          for (int t = 0; t < (NA == 1 ? kTok : 1); ++t) {
-            const int rr = te.row0 + t;
-            if (t < nt && rr < a.total_rows) {
-              const float4* hp =
-                  reinterpret_cast<const float4*>(a.binv + static_cast<size_t>(rr) * G + g8);
-              const float4 v0 = __ldg(hp), v1 = __ldg(hp + 1);
-              hb[t][0] = v0.x;
-              hb[t][1] = v0.y;
-              hb[t][2] = v0.z;
-              hb[t][3] = v0.w;
-              hb[t][4] = v1.x;
-              hb[t][5] = v1.y;
-              hb[t][6] = v1.z;
-              hb[t][7] = v1.w;
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) hb[t][i] = 0.f;
-            }
-          }
-        }
 #pragma unroll
         for (int gi = 0; gi < 8; gi += kGroupsPerSync) {
           if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ring], rph, ab))) {
@@ -583,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float pv = (__uint_as_float(v[jj][3 * t]) +
                                   __uint_as_float(v[jj][3 * t + 1])) +
                                  __uint_as_float(v[jj][3 * t + 2]);
-                acc0[t] = fmaf(sa * hb[NA == 1 ? t : 0][gi + jj], pv, acc0[t]);
+                const float hbv = s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gi + jj : 0];
+                acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
               }
             }
           }
