@@ -69,7 +69,8 @@ constexpr int kCodeTileBytes = kBM * (kRawK / 2);  // 16 KB packed codes per mat
 constexpr int kBRows = 16;
 constexpr int kBTileBytes = kBRows * kSlotK;       // 2 KB
 constexpr int kBStages = 8;
-constexpr int kGroupsPerSync = 2;                  // groups per accumulator handshake
+constexpr int kGroupsPerSync = 4;                  // groups per accumulator handshake (a slot)
+constexpr int kGroupsPerLoad = 2;                  // groups per TMEM load batch of the epilogue
 constexpr int kTmemCols = 512;
 constexpr int kBarBytes = 1024;
 constexpr int kThreads = 480;
@@ -518,68 +519,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t tq =
+          const uint32_t tq0 =
               tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ring * Cfg::kEntryCols;
-          if (NA == 2) {
-            if (2 * nt <= 8) {  // at most 4 tokens: columns 0..7 of each accumulator
-              uint32_t v[kGroupsPerSync][2][8];
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-                tmem_ld_32x32b_x8(tq + jj * 32, v[jj][0]);
-                tmem_ld_32x32b_x8(tq + jj * 32 + 16, v[jj][1]);
-              }
-              tmem_ld_wait();
-              tc_fence_before_sync();
-              mbar_arrive(&acc_empty[ring]);
+          for (int gl = 0; gl < kGroupsPerSync; gl += kGroupsPerLoad) {
+            const uint32_t tq = tq0 + gl * Cfg::kGroupCols;
+            const int gb = gi + gl;  // first group of this load batch within the eight
+            if (NA == 2) {
+              if (2 * nt <= 8) {  // at most 4 tokens: columns 0..7 of each accumulator
+                uint32_t v[kGroupsPerLoad][2][8];
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-                const float sa = scale_of(s0, gi + jj), sb = scale_of(s1, gi + jj);
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                  tmem_ld_32x32b_x8(tq + jj * 32, v[jj][0]);
+                  tmem_ld_32x32b_x8(tq + jj * 32 + 16, v[jj][1]);
+                }
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                  acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
-                  acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                  const float sa = scale_of(s0, gb + jj), sb = scale_of(s1, gb + jj);
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) {
+                    acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
+                    acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                  }
+                }
+              } else {
+                uint32_t v[kGroupsPerLoad][2][16];
+#pragma unroll
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                  tmem_ld_32x32b_x16(tq + jj * 32, v[jj][0]);
+                  tmem_ld_32x32b_x16(tq + jj * 32 + 16, v[jj][1]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                  const float sa = scale_of(s0, gb + jj), sb = scale_of(s1, gb + jj);
+#pragma unroll
+                  for (int c = 0; c < 16; ++c) {
+                    acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
+                    acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                  }
                 }
               }
             } else {
-              uint32_t v[kGroupsPerSync][2][16];
+              uint32_t v[kGroupsPerLoad][16];
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-                tmem_ld_32x32b_x16(tq + jj * 32, v[jj][0]);
-                tmem_ld_32x32b_x16(tq + jj * 32 + 16, v[jj][1]);
-              }
+              for (int jj = 0; jj < kGroupsPerLoad; ++jj) tmem_ld_32x32b_x16(tq + jj * 16, v[jj]);
               tmem_ld_wait();
-              tc_fence_before_sync();
-              mbar_arrive(&acc_empty[ring]);
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-                const float sa = scale_of(s0, gi + jj), sb = scale_of(s1, gi + jj);
+              for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                const float sa = scale_of(s0, gb + jj);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
-                  acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+                for (int t = 0; t < kTok; ++t) {
+                  const float pv = (__uint_as_float(v[jj][3 * t]) +
+                                    __uint_as_float(v[jj][3 * t + 1])) +
+                                   __uint_as_float(v[jj][3 * t + 2]);
+                  const float hbv =
+                      s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gb + jj : 0];
+                  acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
                 }
               }
             }
-          } else {
-            uint32_t v[kGroupsPerSync][16];
-#pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) tmem_ld_32x32b_x16(tq + jj * 16, v[jj]);
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&acc_empty[ring]);
-#pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              const float sa = scale_of(s0, gi + jj);
-#pragma unroll
-              for (int t = 0; t < kTok; ++t) {
-                const float pv = (__uint_as_float(v[jj][3 * t]) +
-                                  __uint_as_float(v[jj][3 * t + 1])) +
-                                 __uint_as_float(v[jj][3 * t + 2]);
-                const float hbv = s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gi + jj : 0];
-                acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
-              }
-            }
           }
+          tc_fence_before_sync();
+          mbar_arrive(&acc_empty[ring]);
           if (++ring == Cfg::kAccRing) {
             ring = 0;
             rph ^= 1u;

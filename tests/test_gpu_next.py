@@ -103,6 +103,31 @@ def test_accumulate_adds_to_residual(decode, flags):
         assert np.array_equal(out, _run(decode, x, flags, out_init=resid))
 
 
+@pytest.fixture(scope="module")
+def decode4_64():
+    return DeviceLayer(make_inputs(synthetic.WORKLOADS["decode_int4"]))
+
+
+@pytest.mark.parametrize("flags", [DET, ACC, ACC | DET])
+def test_int4_decode_64_modes(decode4_64, flags):
+    # 64 tokens on the 8-bit Int4 path: the shared expert's 64 rows span 8
+    # gate/up entries and 13 down entries; the deterministic mode stores the
+    # down rows and combines them in a fixed order, the accumulate mode adds
+    # the layer into the residual already in out.
+    layer = decode4_64
+    x = layer.inp.x[:64]
+    resid = None
+    if flags & ACC:
+        rng = np.random.default_rng(11)
+        resid = rng.standard_normal((64, layer.wl.H)).astype(np.float32)
+    out = _run(layer, x, flags, out_init=resid)
+    ref = _ref(layer, x)
+    got = out - (resid.astype(np.float64) if resid is not None else 0.0)
+    assert rel_max_err(got, ref) <= TOL["int4"]
+    if flags & DET:
+        assert np.array_equal(out, _run(layer, x, flags, out_init=resid))
+
+
 # ------------------------------------------------------------------ dense FFN
 
 def _dense_case(fmt, I, seed):
