@@ -443,8 +443,10 @@ def run_ours(args, wl, rank, world, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
-                     "int4 weights dequantised to fp16, fp32 accumulate",
+            "dtype": ("bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
+                      "int4 weights as e5m2 (n - 8) x e4m3 activation planes, scale per group "
+                      "after the MMA, fp32 accumulate" if wl.T <= 64 else
+                      "int4 weights dequantised to fp16, fp32 accumulate"),
             "data": "synthetic (seeded generator; random-init weights)",
             "config": config_of(wl, world, args),
             "roofline": {"bound": "hbm", "kernel": "gateup_swiglu (tcgen05 grouped gate/up)",
