@@ -80,8 +80,9 @@ def test_deterministic_decode(decode, T):
     assert rel_max_err(a[sample], _ref(decode, x[sample])) <= TOL["bf16"]
 
 
-def test_deterministic_int4(decode4):
-    x = decode4.inp.x
+@pytest.mark.parametrize("T", [1, 16])
+def test_deterministic_int4(decode4, T):
+    x = decode4.inp.x[:T]
     a = _run(decode4, x, DET)
     b = _run(decode4, x, DET)
     assert np.array_equal(a, b)
