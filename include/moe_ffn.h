@@ -169,6 +169,10 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
  * routing weight and adds into out (fp32 [T][H]), with the shared expert run
  * as one more group of weight 1.  By default out is overwritten and the fp32
  * additions into it are atomic, so the last bits may differ run to run.
+ * Int4 weights up to 64 tokens run on 8-bit tensor-core operands: the codes
+ * as e5m2 (n - 8, exact), x and h as e4m3 planes under power-of-two scales
+ * (x exactly; h to 12 significant bits), each group's scale applied to its
+ * fp32 partial product; larger T expands the weights to fp16 operands.
  * Flags (moe_dims.flags):
  *   MOE_FLAG_DETERMINISTIC  the down GEMM stores unweighted rows into the
  *       workspace and a fixed-order combination (slot 0..top_k-1, then the
@@ -190,7 +194,8 @@ moe_status moe_ffn_forward(const moe_dims* d, const void* x, const void* w_route
  *   0 router logits + top-k (for T <= 16 also the permutation, run by the
  *     top-k kernel's last CTA)   1 permutation (one CTA for T <= 128; count,
  *     scan, scatter above) and the gather of x_perm (bf16 weights and T <= 8:
- *     none; the gate/up GEMM gathers its token rows from x itself)
+ *     none; the gate/up GEMM gathers its token rows from x itself; Int4
+ *     weights and T <= 64: the split of each row into two e4m3 planes)
  *   2 grouped gate/up + SwiGLU   3 grouped down + weighted scatter-add
  * Each ev[i] is a cudaEvent_t created by the caller (NULL entries are skipped).
  * When `stream` is being captured into a CUDA graph the records are captured

@@ -37,19 +37,21 @@
 //                    elements per raw stage
 //   warp 1           TMEM allocation; lane 0 issues tcgen05.mma kind::f8f6f4
 //                    (A e5m2, B e4m3)
-//   warps 2..5       epilogue: per two scale groups, tcgen05.ld of their
-//                    accumulators, scale and add; after the last group the
-//                    SwiGLU and the h planes (gate/up) or the scatter-add /
-//                    row store (down)
+//   warps 2..5       epilogue: per operand slot (four scale groups),
+//                    tcgen05.ld of their accumulators in two batches, scale
+//                    and add; after the last group the SwiGLU and the h
+//                    planes (gate/up) or the scatter-add / row store (down)
 //   warps 6..13      dequantisers, two threads per weight row (one per matrix
 //                    for gate/up, one per two of a slot's four groups for
 //                    down): code words -> e5m2 bytes (fp16 mask-and-or, one
 //                    half2 subtract, one byte permute per four codes), written
 //                    into the 128-byte-swizzled operand tile
 //   warp 14, lane 0  activation producer: TMA of the e4m3 planes
-// Accumulators: a ring of two-group entries over all 512 TMEM columns; the
-// MMA thread commits and the epilogue warps release one entry per two groups.
-// Every wait is bounded as in the other GEMM kernels.
+// Accumulators: a ring of four-group entries over all 512 TMEM columns; the
+// MMA thread commits and the epilogue warps release one entry per operand
+// slot (a handshake every two groups cost ~12 % more: issuing the small MMAs
+// is what bounds these kernels).  Every wait is bounded as in the other GEMM
+// kernels.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
