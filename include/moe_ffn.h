@@ -171,7 +171,8 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
  * additions into it are atomic, so the last bits may differ run to run.
  * Int4 weights up to 64 tokens run on 8-bit tensor-core operands: the codes
  * as e5m2 (n - 8, exact), x and h as e4m3 planes under power-of-two scales
- * (x exactly; h to 12 significant bits), each group's scale applied to its
+ * (x exactly; h within 2^-12 relative near each 32-feature group's largest
+ * |h| and 2^-17 of it absolute below), each group's scale applied to its
  * fp32 partial product; larger T expands the weights to fp16 operands.
  * Flags (moe_dims.flags):
  *   MOE_FLAG_DETERMINISTIC  the down GEMM stores unweighted rows into the

@@ -21,9 +21,11 @@
 // two scale, each plane the rounding remainder of the ones before:
 //   gate/up: x as hi + lo (bf16's 8 significant bits split exactly into
 //            4 + 4), one scale per token row;
-//   down:    h as hi + mid + lo (12 significant bits, one more than fp16),
-//            one scale per token row and group of 32 features, chosen by the
-//            gate/up epilogue from the largest |h| of the group.
+//   down:    h as hi + mid + lo, one scale per token row and group of 32
+//            features, chosen by the gate/up epilogue from the largest |h| of
+//            the group: 12 significant bits for values within 2^-5 of that
+//            largest |h|, an absolute error below 2^-17 of it for the rest
+//            (where the last plane reaches e4m3's subnormal quantum).
 // Every product is exact in fp32; only fp32 accumulation rounds.
 //
 // B operand: rows P t .. P t + P - 1 are token t's planes (P = 2 or 3), so
