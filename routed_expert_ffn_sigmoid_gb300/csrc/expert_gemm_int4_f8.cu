@@ -690,6 +690,8 @@ cudaError_t f8_dispatch(const Int4F8Launch& L, cudaStream_t s) {
 
 cudaError_t launch_int4_f8_gemm(const Int4F8Launch& L, cudaStream_t s) {
   if (L.K % kRawK != 0 || L.N_out % kBM != 0) return cudaErrorInvalidValue;
+  // down keeps the tile's h scales (K / 32 per token) in static shared memory
+  if (L.na == 1 && L.K / 32 > kMaxGroups) return cudaErrorInvalidValue;
   if (L.na == 2) return f8_dispatch<2, kEpiStoreRows>(L, s);
   if (L.epilogue == kEpiScatterAdd) return f8_dispatch<1, kEpiScatterAdd>(L, s);
   return f8_dispatch<1, kEpiStoreRows>(L, s);

@@ -213,3 +213,16 @@ def test_forward_int4_row_scales(decode4):
     assert rel_max_err(out, ref) <= TOL["int4"]
     # the zero row's output is the shared expert and routed experts of x = 0: 0
     assert np.abs(out[0]).max() == 0.0
+
+
+@pytest.mark.parametrize("H,I,T", [(256, 4096, 24), (256, 4352, 24), (12288, 256, 9)])
+def test_forward_int4_largest_shapes_of_each_path(H, I, T):
+    # I = 4096 is the largest intermediate size the 8-bit decode kernels take
+    # (down keeps I / 32 = 128 h scales per token in shared memory); I = 4352
+    # runs the fp16-operand kernels at the same token count; H = 12288 is the
+    # largest hidden size the layer accepts.  16 experts: several tile entries
+    # per expert, each with a ragged tail.
+    wl = synthetic.Workload(f"int4_H{H}_I{I}", T, H, 16, I, I, 8, "int4", 41, tokens=(T,))
+    layer = DeviceLayer(make_inputs(wl))
+    out = layer.forward(layer.inp.x)
+    assert rel_max_err(out, _ref(layer, layer.inp.x)) <= TOL["int4"]
