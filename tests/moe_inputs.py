@@ -31,7 +31,10 @@ class LayerInputs:
 
 
 def boundary_gap(z: np.ndarray, k: int) -> np.ndarray:
-    """z_(k) - z_(k+1) per row (k-th and k+1-th largest)."""
+    """z_(k) - z_(k+1) per row (k-th and k+1-th largest); infinite when every
+    expert is selected (k = E), which leaves no boundary to keep clear."""
+    if k >= z.shape[1]:
+        return np.full(z.shape[0], np.inf)
     part = -np.partition(-z, (k - 1, k), axis=1)
     return part[:, k - 1] - part[:, k]
 

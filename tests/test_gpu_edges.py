@@ -1,6 +1,7 @@
 """GPU edge cases of the routing and the layer: exact ties at the top-k
-boundary, every logit tied, and the largest expert count and top-k the
-library accepts, each against the oracle.
+boundary, every logit tied, the largest expert count and top-k the library
+accepts, and the two degenerate selections (every expert, or one), each
+against the oracle.
 
 Ties: the pages ask for a deterministic top-k, which the oracle reads as
 "equal scores go to the lower expert index" ("feat(glm53): add
@@ -44,9 +45,12 @@ def _forward(wl, x, w_router, b_router, ex, sh, T):
     dims = moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt)
     ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
     out = torch.full((T, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+    # the weight structs hold bare device pointers: the uploaded tensors must
+    # stay referenced until the layer has run, or the allocator hands their
+    # memory to the next upload before the kernels read it
+    ex_dev, sh_dev = upload_matrices(ex), upload_matrices(sh)
     moe.moe_ffn_forward(dims, dev_u16(x), dev_u16(w_router), torch.from_numpy(b_router).cuda(),
-                        weights_struct(upload_matrices(ex)), weights_struct(upload_matrices(sh)),
-                        out, ws)
+                        weights_struct(ex_dev), weights_struct(sh_dev), out, ws)
     assert moe.moe_workspace_status(ws) == moe.MOE_OK
     return out.cpu().numpy()
 
@@ -97,3 +101,30 @@ def test_largest_expert_count_and_top_k():
     assert np.array_equal(np.sort(idx, axis=1), np.sort(r_idx, axis=1))
     out = _forward(wl, inp.x, inp.w_router, inp.b_router, inp.experts, inp.shared, wl.T)
     assert rel_max_err(out, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("T", [24, 300])
+@pytest.mark.parametrize("fmt,E,k", [("bf16", 8, 8), ("bf16", 16, 1), ("int4", 8, 8),
+                                     ("int4", 16, 1)])
+def test_every_expert_or_a_single_expert_selected(fmt, E, k, T):
+    """top_k = E: every expert is selected, each token is a row of every
+    group, and the weights are the sigmoids over all experts divided by their
+    sum.  top_k = 1: the one selected expert gets weight exactly 1 (the
+    renormalisation divides a score by itself)."""
+    I = 64 if fmt == "bf16" else 256  # Int4 needs multiples of 256
+    wl = synthetic.Workload(f"edge_{fmt}_E{E}_k{k}", T, 256, E, I, I, k, fmt, 9, tokens=(T,))
+    inp = make_inputs(wl)
+    ref, r_idx, _ = oracle.moe_forward(inp.x, inp.w_router, inp.b_router, inp.experts,
+                                       inp.shared, fmt, top_k=k)
+    idx, w = _route(wl, inp.x, inp.w_router, inp.b_router, T)
+    assert np.array_equal(np.sort(idx, axis=1), np.sort(r_idx, axis=1))
+    if k == E:
+        assert np.array_equal(np.sort(idx, axis=1), np.broadcast_to(np.arange(E), idx.shape))
+        z = oracle.router_logits(inp.x, inp.w_router, inp.b_router).astype(np.float64)
+        s = 1.0 / (1.0 + np.exp(-z))
+        want = np.take_along_axis(s / s.sum(axis=1, keepdims=True), idx.astype(np.int64), axis=1)
+        np.testing.assert_allclose(w, want, rtol=1e-5)
+    else:
+        assert np.all(w == np.float32(1.0))
+    out = _forward(wl, inp.x, inp.w_router, inp.b_router, inp.experts, inp.shared, T)
+    assert rel_max_err(out, ref) <= TOL[fmt]
