@@ -139,8 +139,14 @@ def make_dims(T: int, H: int, E: int, I: int, I_shared: int | None = None, top_k
 
 
 def make_weights(gate, up, down, gate_scale=None, up_scale=None, down_scale=None) -> MoeWeights:
-    return MoeWeights(_ptr(gate), _ptr(up), _ptr(down), _ptr(gate_scale), _ptr(up_scale),
-                      _ptr(down_scale))
+    """The weight-pointer struct of a stack.  It keeps the tensors it points
+    into referenced for as long as it lives, so a struct built from
+    temporaries stays valid until the calls that use it are enqueued (later
+    reuse of the memory by torch's allocator is ordered on the stream)."""
+    w = MoeWeights(_ptr(gate), _ptr(up), _ptr(down), _ptr(gate_scale), _ptr(up_scale),
+                   _ptr(down_scale))
+    w._tensors = (gate, up, down, gate_scale, up_scale, down_scale)
+    return w
 
 
 def moe_workspace_size(dims: MoeDims) -> int:

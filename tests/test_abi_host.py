@@ -126,3 +126,22 @@ def test_missing_library_raises(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         moe.lib()
+
+
+def test_weights_struct_keeps_its_tensors_alive():
+    # the struct holds bare pointers; the tensors behind them must live as
+    # long as it does, also when they were passed in as temporaries
+    import gc
+    import weakref
+    torch = pytest.importorskip("torch")
+    made = [torch.zeros(64, dtype=torch.int16) for _ in range(6)]
+    refs = [weakref.ref(t) for t in made]
+    ptrs = [t.data_ptr() for t in made]
+    w = moe.make_weights(*made)
+    del made
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    assert [w.gate, w.up, w.down, w.gate_scale, w.up_scale, w.down_scale] == ptrs
+    del w
+    gc.collect()
+    assert all(r() is None for r in refs)
