@@ -203,7 +203,11 @@ def parse():
                     help="time eager layer calls instead of CUDA graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
-    return ap.parse_args()
+    args = ap.parse_args()
+    # at least three untimed warm-up steps before any timed region; the JSON
+    # line reports the number actually run
+    args.warmup = max(args.warmup, 3)
+    return args
 
 
 def dist_env():
