@@ -30,10 +30,12 @@
  * - Device pointers must be 16-byte aligned.
  * - bf16 / fp16 values are IEEE bit patterns in uint16 storage.
  * - T == 0 is a no-op: the call returns MOE_OK and reads or writes nothing.
- * - Shapes: T >= 0 tokens; H hidden size, multiple of 128; E routed experts,
- *   top_k <= E <= 512; I expert intermediate size, multiple of 64;
- *   I_shared == I; 1 <= top_k <= 16.  Other shapes return
- *   MOE_ERR_UNSUPPORTED.  The device must be sm_103 (GB300).
+ * - Shapes: T >= 0 tokens with (top_k+1)*T <= 2^30; H hidden size, a
+ *   multiple of 128 up to 12288; E routed experts, top_k <= E <= 512; I
+ *   expert intermediate size, multiple of 64; I_shared == I;
+ *   1 <= top_k <= 16.  Int4 weights also need H and I to be multiples of 256.
+ *   Other shapes return MOE_ERR_UNSUPPORTED.  The device must be sm_103
+ *   (GB300).
  * - There is no CPU fallback: without a suitable GPU every call fails.
  *
  * Matrix layouts ("nn.Linear", output-major, reduction dim contiguous):
@@ -147,7 +149,9 @@ moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, const void* x
  * unweighted.  Gate/up and down run on tcgen05 tensor cores with fp32
  * accumulation; the clamped SwiGLU ("gate (-inf, 10] -> SiLU, up [-10, 10]",
  * lucebox PR #1, Architecture) is fused into the gate/up epilogue.
- * x_perm and offsets as produced by moe_permute.
+ * x_perm and offsets as produced by moe_permute.  Int4 weights run on fp16
+ * operands here at every T (the 8-bit path of moe_ffn_forward needs the e4m3
+ * planes that only the fused call prepares).
  */
 moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* offsets,
                           const moe_weights* experts, const moe_weights* shared, float* y_perm,
