@@ -56,8 +56,14 @@ def test_workspace_size(L):
                 moe.make_dims(8, 256, 600, 64), moe.make_dims(8, 256, 288, 64, top_k=17),
                 moe.make_dims(-1, 256, 288, 64), moe.make_dims(8, 256, 288, 64, I_shared=128),
                 moe.make_dims(8, 256, 4, 64, top_k=8), moe.make_dims(8, 256, 288, 64, fmt=7),
-                moe.make_dims(8, 256, 288, 64, flags=4)):
+                moe.make_dims(8, 256, 288, 64, flags=4), moe.make_dims(8, 12416, 288, 64),
+                moe.make_dims(8, 384, 288, 256, fmt="int4"),
+                moe.make_dims((1 << 30) // 9 + 1, 256, 288, 64)):
         assert moe.moe_workspace_size(bad) == 0
+    # the limits themselves are accepted
+    for ok in (moe.make_dims(8, 12288, 288, 64), moe.make_dims(8, 512, 288, 256, fmt="int4"),
+               moe.make_dims((1 << 30) // 9, 256, 288, 64)):
+        assert moe.moe_workspace_size(ok) > 0
     # the deterministic mode keeps (top_k+1)*T*H fp32 rows in the workspace
     det = moe.make_dims(64, 4096, 288, 1536, flags=moe.MOE_FLAG_DETERMINISTIC)
     assert moe.moe_workspace_size(det) - big >= rows * 4096 * 4
