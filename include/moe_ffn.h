@@ -33,7 +33,10 @@
  * - Shapes: T >= 0 tokens with (top_k+1)*T <= 2^30; H hidden size, a
  *   multiple of 128 up to 12288; E routed experts, top_k <= E <= 512; I
  *   expert intermediate size, multiple of 64; I_shared == I;
- *   1 <= top_k <= 16.  Int4 weights also need H and I to be multiples of 256.
+ *   1 <= top_k <= 16.  Int4 weights also need H and I to be multiples of 256,
+ *   and token values within fp16's range (|x| <= 65504) wherever the tokens
+ *   enter as fp16 (moe_permute / moe_expert_ffn, moe_dense_ffn, and
+ *   moe_ffn_forward above 64 tokens); larger values are not checked.
  *   Other shapes return MOE_ERR_UNSUPPORTED.  The device must be sm_103
  *   (GB300).
  * - There is no CPU fallback: without a suitable GPU every call fails.
@@ -131,7 +134,8 @@ moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_route
  *   gather   [(top_k+1)*T] int32: token of each row (ascending within a group)
  *   row_of   [T][top_k] int32: row holding (t, j)
  *   x_perm   [(top_k+1)*T][H]: x[gather[r]] -- bf16 for MOE_W_BF16; for
- *            MOE_W_INT4_G32 fp16 (exact conversion of the bf16 input) in the
+ *            MOE_W_INT4_G32 fp16 (the bf16 input converted: exact in fp16's
+ *            normal range, within 2^-25 below it) in the
  *            Int4 kernels' operand order: within every aligned group of 8
  *            columns, position p holds column (0, 4, 1, 5, 2, 6, 3, 7)[p].
  *            The order is what lets the kernels expand packed codes with
@@ -180,8 +184,9 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
  * additions into it are atomic, so the last bits may differ run to run.
  * Int4 weights up to 64 tokens run on 8-bit tensor-core operands: the codes
  * as e5m2 (n - 8, exact), x and h as e4m3 planes under power-of-two scales
- * (x exactly; h within 2^-12 relative near each 32-feature group's largest
- * |h| and 2^-17 of it absolute below), each group's scale applied to its
+ * (x exactly for entries at least 2^-9 of their row's largest |x|, within
+ * 2^-17 of it below; h within 2^-12 relative near each 32-feature group's
+ * largest |h| and 2^-17 of it absolute below), each group's scale applied to its
  * fp32 partial product; larger T expands the weights to fp16 operands.
  * Flags (moe_dims.flags):
  *   MOE_FLAG_DETERMINISTIC  the down GEMM stores unweighted rows into the

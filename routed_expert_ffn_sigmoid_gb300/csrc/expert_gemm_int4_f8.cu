@@ -19,8 +19,10 @@
 // accumulator of its own, and the epilogue warps add s_g times it into
 // registers.  The activation rows (B) enter as e4m3 planes under a power-of-
 // two scale, each plane the rounding remainder of the ones before:
-//   gate/up: x as hi + lo (bf16's 8 significant bits split exactly into
-//            4 + 4), one scale per token row;
+//   gate/up: x as hi + lo, one scale per token row: bf16's 8 significant
+//            bits split exactly into 4 + 4 for values at least 2^-9 of the
+//            row's largest |x|; below that lo reaches e4m3's subnormal
+//            quantum and the error stays under 2^-17 of the largest |x|;
 //   down:    h as hi + mid + lo, one scale per token row and group of 32
 //            features, chosen by the gate/up epilogue from the largest |h| of
 //            the group: 12 significant bits for values within 2^-5 of that

@@ -19,38 +19,13 @@ and e5m2 (OCP FP8 formats: e4m3 bias 7, 3 mantissa bits, max 448; e5m2 bias
 
 import numpy as np
 
-
-def round_fp8(y, mant_bits, emin, max_finite):
-    """Round float64 values to the nearest representable FP8 value (ties to
-    even), saturating at +-max_finite; emin is the smallest normal exponent."""
-    y = np.asarray(y, dtype=np.float64)
-    a = np.abs(y)
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(e, emin)  # subnormals share the quantum of the smallest normal
-    q = np.exp2(e - mant_bits)
-    r = np.round(a / q) * q  # numpy rounds half to even
-    r = np.minimum(r, max_finite)
-    return np.sign(y) * r
-
-
-def e4m3(y):
-    return round_fp8(y, 3, -6, 448.0)
-
-
-def e5m2(y):
-    return round_fp8(y, 2, -14, 57344.0)
+from fp8_model import e4m3, e5m2, row_sigma
 
 
 def all_bf16_finite():
     bits = np.arange(1 << 16, dtype=np.uint32)
     f = (bits << 16).view(np.float32)
     return f[np.isfinite(f)].astype(np.float64)
-
-
-def row_sigma(mx):
-    # sigma = 2^(8 - e) with mx = f 2^e, f in [0.5, 1): mx sigma in [128, 256)
-    _, e = np.frexp(mx)
-    return np.exp2(8.0 - e)
 
 
 def test_model_matches_known_encodings():
