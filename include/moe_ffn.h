@@ -143,8 +143,10 @@ moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_route
  * The grouping that feeds the per-expert matmuls ("ggml_mul_mat_id for
  * gate/up/down", lucebox PR #1, "MoE FFN" section).
  * Precondition: every topk_idx entry lies in [0, E), as moe_router_topk
- * writes them.  The ids are on the device and are not validated; other
- * values give undefined results.
+ * writes them.  The ids are on the device and no error is reported for
+ * others: such a pair gets no row (row_of = -1, which moe_combine skips),
+ * the other results are undefined, and nothing is written outside the
+ * arrays passed in.
  */
 moe_status moe_permute(const moe_dims* d, const int32_t* topk_idx, const void* x,
                        int32_t* offsets, int32_t* gather, int32_t* row_of, void* x_perm, void* ws,
@@ -170,8 +172,9 @@ moe_status moe_expert_ffn(const moe_dims* d, const void* x_perm, const int32_t* 
  *   out[t] = sum_{j=0..top_k-1} topk_w[t][j] * y_perm[row_of[t][j]] + y_perm[top_k*T + t]
  * out fp32 [T][H] is overwritten, or, with MOE_FLAG_ACCUMULATE, added to
  * (its entry value first, then the slots in order).  Bitwise reproducible.
- * Precondition: row_of as moe_permute writes it, every entry in
- * [0, (top_k+1)*T); the rows are not validated on the device.
+ * Precondition: row_of as moe_permute writes it.  A slot whose row lies
+ * outside [0, (top_k+1)*T) (moe_permute writes -1 for an out-of-range
+ * expert id) is skipped.
  */
 moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* row_of,
                        const float* topk_w, float* out, moe_stream_t stream);

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       float4 acc = accumulate ? reinterpret_cast<const float4*>(out + static_cast<size_t>(t) * H)[c]
                               : make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < k; ++j) {
+        if (rows[j] < 0 || rows[j] >= (k + 1) * T) continue;  // a pair without a row
         const float4 v = reinterpret_cast<const float4*>(y + static_cast<size_t>(rows[j]) * H)[c];
         acc.x = fmaf(wt[j], v.x, acc.x);
         acc.y = fmaf(wt[j], v.y, acc.y);

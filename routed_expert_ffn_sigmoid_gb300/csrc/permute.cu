@@ -126,7 +126,10 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* __rest
   for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
     const int tl = i / k;
     const int e = ib[i];
-    if (e < 0 || e >= E) continue;
+    if (e < 0 || e >= E) {  // an out-of-range id gets no row
+      row_of[static_cast<size_t>(t0) * k + i] = -1;
+      continue;
+    }
     int rank = __popc(bits[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
     for (int wd = 0; wd < (tl >> 5); ++wd) rank += __popc(bits[e][wd]);
     const int r = base[e] + rank;
@@ -169,12 +172,17 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int seg_chunks = H / 8 / segs;
+  const int rows = (k + 1) * T;
   for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < T * segs; item += warps) {
     const int t = item / segs, c0 = (item % segs) * seg_chunks;
     uint4* dst[kMaxTopK + 1];
 #pragma unroll
     for (int j = 0; j <= kMaxTopK; ++j) {
-      const int r = j < k ? row_of[static_cast<size_t>(t) * k + j] : k * T + t;
+      // a row outside the buffer (row_of = -1: an out-of-range expert id) is
+      // clamped into it, so the write stays in bounds; the rows' contents are
+      // then as undefined as the results are for such ids
+      const int r = j < k ? min(max(row_of[static_cast<size_t>(t) * k + j], 0), rows - 1)
+                          : k * T + t;
       dst[j] = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
