@@ -58,3 +58,10 @@ def test_two_bf16_planes_of_h_are_needed(expert):
     two = rel_max_err(((hi + lo) @ W["down"].T).astype(np.float32), ref)
     assert one > 2e-3  # a single bf16 plane fails the bf16 tolerance (measured ~8e-3)
     assert two <= 1e-4  # hi + lo: measured ~1.1e-5
+
+
+def test_a_bf16_output_would_fail_the_tolerance(expert):
+    # the reading that the layer output is fp32: rounding the exact expert
+    # output to bf16 alone gives about 1e-2 of RMS (max err / RMS)
+    _, _, ref = expert
+    assert rel_max_err(bf16_round(ref.astype(np.float32)), ref) > 2e-3
