@@ -170,6 +170,20 @@ def _shape():
     return d["routed_experts"], d["top_k"]
 
 
+def test_router_summation_order_stays_far_below_the_boundary_gap():
+    # the inputs keep the 8th / 9th logit gap >= GAP so that every fp32
+    # summation order selects the same experts; at the decode shape the
+    # oracle's in-order fp32 logits are within 1.1e-5 of an fp64 sum
+    from moe_inputs import GAP
+    wl = synthetic.WORKLOADS["decode_bf16"]
+    wr, b = synthetic.gen_router(wl)
+    x = synthetic.gen_x(wl, T=64)
+    z = oracle.router_logits(x, wr, b).astype(np.float64)
+    xf = synthetic.bf16_bits_to_f32(x).astype(np.float64)
+    wf = synthetic.bf16_bits_to_f32(wr).astype(np.float64)
+    assert np.abs(z - (xf @ wf.T + b)).max() < GAP / 20
+
+
 def test_topk_orders_and_ties():
     E, k = _shape()
     z = np.arange(E, dtype=np.float32)[None, :]
