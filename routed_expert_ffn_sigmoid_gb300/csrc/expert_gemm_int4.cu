@@ -4,11 +4,12 @@
 // Weights use the grouped fmt=4 Int4 format decoded as offset-binary,
 // value = (nibble - 8) * scale ("feat(glm53): add device-resident HIP backend
 // for MI350P", section "Key changes"), with one bf16 scale per 32 reduction
-// elements.  (nibble - 8) * scale is exact in fp16 for every scale that fp16
-// represents (a 4-bit integer times an 8-bit significand fits fp16's 11), so
-// the fp16 operand equals the decoded weight and the only rounding left is
-// the fp32 accumulation.  Activations arrive as fp16 (x rows converted
-// exactly from bf16 by the permutation; h written as fp16 by gate/up).
+// elements.  (nibble - 8) * scale is exact in fp16 while the product stays
+// in fp16's normal range (nibble - 8 has at most 3 significant bits and a
+// bf16 scale 8, within fp16's 11), so the fp16 operand equals the decoded
+// weight and the only rounding left is the fp32 accumulation.  Activations
+// arrive as fp16 (x rows converted from bf16 by the permutation, exactly in
+// fp16's normal range; h written as fp16 by gate/up).
 //
 // CTA = 15 warps, persistent over the same flat tile list as the bf16 path:
 //   warp 0, lane 0   raw producer: TMA of packed codes (128-byte swizzle) and
@@ -105,7 +106,8 @@ __device__ __forceinline__ float clamped_swiglu(float g, float u) {
 // (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + e0, 1024 + e4), and
 // (w & 0x00F000F0) | 0x54005400 is (64 + e1, 64 + e5), the nibble sitting four
 // bits up where the ulp of 64 is 1/16.  Subtracting 1032 (or 72) leaves the
-// integer e - 8 exactly; one multiply by the group scale rounds nothing.
+// integer e - 8 exactly; one multiply by the group scale rounds nothing
+// while the product stays in fp16's normal range.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
   const uint32_t w8 = w >> 8;
   const uint32_t p[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
