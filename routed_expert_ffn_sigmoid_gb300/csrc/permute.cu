@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
     for (int c = c0 + lane; c < c0 + seg_chunks; c += 32) {
       uint4 v = __ldg(src + c);
       if (kToFp16) {
-        // exact bf16 -> fp16, the 8 columns stored in the Int4 kernels'
-        // operand order 0, 4, 1, 5, 2, 6, 3, 7
+        // bf16 -> fp16 (exact in fp16's normal range), the 8 columns stored
+        // in the Int4 kernels' operand order 0, 4, 1, 5, 2, 6, 3, 7
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         float e[8];
 #pragma unroll
