@@ -151,3 +151,27 @@ def test_weights_struct_keeps_its_tensors_alive():
     del w
     gc.collect()
     assert all(r() is None for r in refs)
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_is_plain_c_and_cxx(tmp_path, lang, std):
+    # the boundary is a C ABI: the header alone must compile as strict C and
+    # as C++, with no CUDA or torch headers
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text(
+        '#include "moe_ffn.h"\n'
+        "size_t need(const moe_dims* d) { return moe_workspace_size(d); }\n"
+        "int version(void) { return moe_abi_version() == MOE_FFN_ABI_VERSION; }\n"
+        "moe_status fwd(const moe_dims* d, const moe_weights* w, float* out, void* ws, size_t n,\n"
+        "               moe_stream_t s) {\n"
+        "  return moe_ffn_forward(d, 0, 0, 0, w, w, out, ws, n, s);\n"
+        "}\n")
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-c",
+                        "-I", os.path.dirname(HEADER), str(src), "-o", str(tmp_path / "use.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
