@@ -168,17 +168,22 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle
 
 def oracle_sample(wl, x, w_router, b_router, experts, shared, budget_s=12.0):
-    """Times the oracle on successive token slices of x until budget_s."""
+    """Times the oracle on successive token slices of x until budget_s.
+
+    The oracle runs its tokens in parallel (one thread per token), so each
+    slice holds as many tokens as it has threads (fewer if x is shorter).
+    Returns (tokens done, seconds, threads used, tokens per slice)."""
     import oracle
     done, t0 = 0, time.perf_counter()
-    chunk = max(1, min(x.shape[0], 8))
+    chunk = max(1, min(x.shape[0], oracle.max_threads()))
     while True:
-        xs = np.ascontiguousarray(x[done % x.shape[0]:done % x.shape[0] + chunk])
+        start = (done // chunk * chunk) % x.shape[0]
+        xs = np.ascontiguousarray(x[start:start + chunk])
         oracle.moe_forward(xs, w_router, b_router, experts, shared, wl.fmt)
         done += xs.shape[0]
         el = time.perf_counter() - t0
         if el >= budget_s:
-            return done, el, oracle.max_threads()
+            return done, el, min(chunk, oracle.max_threads()), chunk
 
 
 # ------------------------------------------------------------------ main
@@ -202,6 +207,10 @@ def parse():
     ap.add_argument("--eager", action="store_true",
                     help="time eager layer calls instead of CUDA graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (every workload's configurations)")
+    ap.add_argument("--per-config-cpu-s", type=float, default=1.5,
+                    help="oracle seconds per per_config entry (0: no oracle timing)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
     # at least three untimed warm-up steps before any timed region; the JSON
@@ -249,11 +258,14 @@ def run_reference(args, wl, rank, world):
     for _ in range(args.warmup):
         pass  # the oracle has no warm state; warm-up steps are not timed
     t_all = 0.0
-    cores = 0
+    import oracle
+    # the oracle runs one thread per token: each step takes as many of the
+    # step's tokens as it has threads
+    n_per_step = min(wl.T, oracle.max_threads())
+    cores = n_per_step
     for s in range(args.steps):
         x = batches[s % N_BATCHES]
-        n = min(x.shape[0], 8)
-        import oracle
+        n = n_per_step
         t0 = time.perf_counter()
         oracle.moe_forward(np.ascontiguousarray(x[:n]), w_router, b_router, experts, shared,
                            wl.fmt)
@@ -261,7 +273,6 @@ def run_reference(args, wl, rank, world):
         per_step.append(dt)
         tokens += n
         t_all += dt
-        cores = oracle.max_threads()
     value = tokens / t_all
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -269,7 +280,8 @@ def run_reference(args, wl, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"first {min(wl.T, 8)} tokens of each step's batch"},
+                             "sample": f"first {n_per_step} tokens of each step's batch "
+                                       f"(one oracle thread per token)"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -436,11 +448,11 @@ def run_ours(args, wl, rank, world, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        n, el, cores = oracle_sample(wl, batches[0], w_router, b_router, experts, shared,
-                                     args.cpu_budget_s)
+        n, el, cores, chunk = oracle_sample(wl, np.concatenate(batches), w_router, b_router,
+                                            experts, shared, args.cpu_budget_s)
         cpu = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} tokens of the same workload (slices of 8 tokens of batch 0), "
-                         f"{el:.1f} s"}
+               "sample": f"{n} tokens of the same workload's x batches, in slices of {chunk} "
+                         f"tokens (one oracle thread per token), {el:.1f} s"}
 
     if rank == 0:
         line = {
@@ -471,9 +483,169 @@ def run_ours(args, wl, rank, world, local):
             "gpu_launches": layer_launches(wl.T, args.deterministic, wl.fmt) * args.steps,
             "clocks": clk.summary(),
         }
+        if (world == 1 and not args.no_per_config and not args.deterministic
+                and not args.accumulate and not args.experts):
+            # every workload's configurations, each timed the same way (graph
+            # replays, L2 flushed outside the events, its own clock record)
+            line["per_config"] = per_config_block(
+                args, dev, (wl.name, (wr, b, exw, shw), w_router, b_router, experts, shared))
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ every workload
+
+# (workload, token counts) of the per-config block, in the order they run
+PER_CONFIG = (("decode_bf16", (1, 8, 32, 64)), ("decode_int4", (1, 8, 32, 64)),
+              ("prefill_bf16", (4096,)), ("skewed_prefill_int4", (16384,)))
+PER_CONFIG_REGION_MS = 300.0  # timed region per entry (long enough for clock samples)
+
+
+def upload_layer(moe, dev, w_router, b_router, experts, shared):
+    import torch
+
+    def up(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t if a.dtype == np.uint8 else t.view(torch.int16)).to(dev)
+
+    ex = {k: up(v) for k, v in experts.items()}
+    sh = {k: up(v) for k, v in shared.items()}
+    exw = moe.make_weights(ex["gate"], ex["up"], ex["down"], ex.get("gate_scale"),
+                           ex.get("up_scale"), ex.get("down_scale"))
+    shw = moe.make_weights(sh["gate"], sh["up"], sh["down"], sh.get("gate_scale"),
+                           sh.get("up_scale"), sh.get("down_scale"))
+    return up(w_router), torch.from_numpy(b_router).to(dev), exw, shw
+
+
+def time_config(moe, dev, wl, layer, host_x, w_router_np, b_router_np, experts_np, shared_np,
+                warmup, cpu_budget_s, hbm_peak, tc_peak, tc_sust):
+    """One per-config entry: CUDA-graph replays of moe_ffn_forward over the
+    workload's seeded x batches, L2 flushed before each replay outside the
+    events, clocks sampled during the timed region; roofline on the layer's
+    algorithmic bytes or flops; the oracle timed on the same workload."""
+    import torch
+
+    wr, b, exw, shw = layer
+    xs = [torch.from_numpy(bt.view(np.int16)).to(dev) for bt in host_x]
+    dims = moe.make_dims(wl.T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, 0)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
+    out = torch.zeros((wl.T, wl.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    distinct = []
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    wts = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device=dev)
+    for x in xs:
+        moe.moe_router_topk(dims, x, wr, b, idx, wts, ws)
+        distinct.append(int(torch.unique(idx).numel()))
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    for bi in range(N_BATCHES):
+        moe.moe_ffn_forward(dims, xs[bi], wr, b, exw, shw, out, ws)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+            moe.moe_ffn_forward(dims, xs[bi], wr, b, exw, shw, out, ws)
+        graphs.append(g)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_warm = []
+    for s_ in range(max(warmup, 3)):
+        flush.zero_()
+        e0.record(stream)
+        graphs[s_ % N_BATCHES].replay()
+        e1.record(stream)
+        e1.synchronize()
+        t_warm.append(e0.elapsed_time(e1))
+    est = min(t_warm)
+    steps = int(min(3000, max(10, PER_CONFIG_REGION_MS / (est + 0.15))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clk:
+        time.sleep(0.3)
+        for s_ in range(steps):
+            flush.zero_()
+            evs[s_][0].record(stream)
+            graphs[s_ % N_BATCHES].replay()
+            evs[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+    st = moe.moe_workspace_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.moe_status_string(st))
+    step_ms = [a.elapsed_time(c) for a, c in evs]
+    ms = statistics.mean(step_ms)
+    mean_distinct = sum(distinct[s_ % N_BATCHES] for s_ in range(steps)) / steps
+    nbytes = statistics.mean(algorithmic_bytes(wl, distinct[s_ % N_BATCHES])
+                             for s_ in range(steps))
+    flops = flops_per_token(wl) * wl.T
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tflops = flops / (ms / 1e3) / 1e12
+    bound = "hbm" if flops / nbytes < tc_peak * 1e12 / (hbm_peak * 1e9) else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_source": "measured hbm_gbs (copy)"}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": tflops / tc_peak, "peak_source": "measured bf16_tflops (burst)",
+                "frac_of_sustained": tflops / tc_sust if tc_sust else None}
+    roof.update({"algorithmic_bytes_per_step": nbytes, "flops_per_step": flops,
+                 "hbm_frac": gbs / hbm_peak, "tc_frac_burst": tflops / tc_peak})
+    cpu = None
+    if cpu_budget_s > 0:
+        n, el, cores, chunk = oracle_sample(wl, np.concatenate(host_x), w_router_np, b_router_np,
+                                            experts_np, shared_np, cpu_budget_s)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of this workload's x batches in slices of {chunk}, "
+                         f"{el:.1f} s"}
+    del graphs, ws, out, flush, xs
+    return {"workload": wl.name, "T": wl.T, "weights": wl.fmt,
+            "config": config_of(wl, 1)["workload"],
+            "steps": steps, "warmup": max(warmup, 3), "ms_per_step": ms,
+            "ms_p10": float(np.percentile(step_ms, 10)), "ms_p90": float(np.percentile(step_ms, 90)),
+            "value": wl.T / (ms / 1e3), "unit": "tokens/s", "GBps": gbs, "TFLOPps": tflops,
+            "distinct_experts_mean": mean_distinct, "roofline": roof,
+            "gpu_launches": layer_launches(wl.T, False, wl.fmt) * steps,
+            "clocks": clk.summary(), "cpu_baseline": cpu}
+
+
+def per_config_block(args, dev, resident=None):
+    """Every workload's configurations timed the same way, one after another.
+
+    resident: (workload name, uploaded layer, host router w, host bias,
+    host experts, host shared) of a stack already on the device, reused for
+    that workload."""
+    import gc
+
+    import torch
+    import routed_expert_ffn_sigmoid_gb300 as moe
+
+    hbm_peak, tc_peak, tc_sust, _ = peaks()
+    entries = []
+    for name, tokens in PER_CONFIG:
+        base = synthetic.WORKLOADS[name]
+        if resident is not None and resident[0] == name:
+            _, layer, w_router, b_router, experts, shared = resident
+        else:
+            resident = None
+            gc.collect()
+            torch.cuda.empty_cache()
+            w_router, b_router = synthetic.gen_router(base)
+            experts = synthetic.gen_experts(base)
+            shared = synthetic.gen_experts(base, shared=True)
+            layer = upload_layer(moe, dev, w_router, b_router, experts, shared)
+        for T in tokens:
+            wl = base.with_tokens(T)
+            x_all = synthetic.gen_x(wl, T=T * N_BATCHES)
+            host_x = [np.ascontiguousarray(x_all[i * T:(i + 1) * T]) for i in range(N_BATCHES)]
+            entries.append(time_config(moe, dev, wl, layer, host_x, w_router, b_router,
+                                       experts, shared, args.warmup, args.per_config_cpu_s,
+                                       hbm_peak, tc_peak, tc_sust))
+        del layer, experts, shared
+        resident = None
+    gc.collect()
+    torch.cuda.empty_cache()
+    return entries
 
 
 def layer_launches(T, deterministic, fmt="bf16"):

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 3
+#define MOE_FFN_ABI_VERSION 4
 
 /* A cudaStream_t, spelled without the CUDA headers. */
 typedef struct CUstream_st* moe_stream_t;
@@ -141,9 +141,11 @@ moe_status moe_router_topk(const moe_dims* d, const void* x, const void* w_route
  *            The order is what lets the kernels expand packed codes with
  *            mask-and-or steps alone; the dot products are unchanged.
  * The grouping that feeds the per-expert matmuls ("ggml_mul_mat_id for
- * gate/up/down", lucebox PR #1, "MoE FFN" section).
- * Precondition: every topk_idx entry lies in [0, E), as moe_router_topk
- * writes them.  The ids are on the device and no error is reported for
+ * gate/up/down", lucebox PR #1, "MoE FFN" section).  Up to 128 tokens one
+ * CTA builds all of it (the same code moe_ffn_forward runs at those sizes);
+ * above, a count, a scan and a scatter kernel.  Both give the same arrays.
+ * Precondition: every topk_idx entry lies in [0, E) and a token's top_k ids
+ * are distinct, as moe_router_topk writes them.  The ids are on the device and no error is reported for
  * others: such a pair gets no row (row_of = -1, which moe_combine skips),
  * the other results are undefined, and nothing is written outside the
  * arrays passed in.
@@ -254,6 +256,65 @@ moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* we
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Where the fused call leaves the layer's routing.  After moe_ffn_forward or
+ * moe_ffn_forward_timed has run on `ws` with these dims, the workspace holds
+ * the router's selection and the permutation the grouped GEMMs consumed
+ * (the top-k of "MoE FFN (REAL routed expert execution)", lucebox PR #1, and
+ * the grouping that feeds its per-expert matmuls), in the layouts of
+ * moe_router_topk and moe_permute:
+ *   topk_idx [T][top_k] int32, topk_w [T][top_k] fp32,
+ *   offsets [E+2] int32, gather [(top_k+1)*T] int32, row_of [T][top_k] int32.
+ * This call only computes addresses inside `ws` (device pointers, read-only
+ * for the caller); it launches and synchronises nothing.  The arrays are
+ * valid once the forward call has completed on its stream and until the
+ * next call that uses the same workspace.  d must be the dims of that
+ * forward call.  T == 0 gives MOE_OK and null pointers.  Useful for
+ * inspecting expert loads (e.g. offsets) and for checking the routing
+ * against a reference.
+ */
+typedef struct moe_routing_view {
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const int32_t* offsets;
+  const int32_t* gather;
+  const int32_t* row_of;
+} moe_routing_view;
+moe_status moe_workspace_routing(const moe_dims* d, const void* ws, size_t ws_bytes,
+                                 moe_routing_view* view);
+
+/*
+ * Tensor parallelism along the expert intermediate dimension: copies slice
+ * `part` of `parts` of a stack's weights into caller-allocated buffers.
+ * The pages' dual-GPU plan places experts on two GPUs ("GLM5next Production
+ * Readiness: Optional Mix Qtypes + Cache Allocation", lucebox PR #2, section
+ * "UNIT 2: Dual-GPU Placement"); this split is the compute form of it.  The
+ * clamped SwiGLU is elementwise in I, so with Is = I / parts, slice p keeps
+ * rows [p Is, (p+1) Is) of gate and up and the same columns of down, and
+ *   layer(x) = sum over p of layer_p(x)
+ * where layer_p is moe_ffn_forward with dims I = I_shared = Is on slice p of
+ * both the routed and the shared stack (routing is computed identically by
+ * every part).  A caller sums the parts' fp32 outputs: on one GPU by
+ * running the parts with MOE_FLAG_ACCUMULATE into one output, across GPUs
+ * with one reduce-scatter or all-reduce of out [T][H].
+ *   d          dims of the FULL layer (I is the full intermediate size)
+ *   n_experts  experts in the stack (d->E for the routed stack, 1 for the
+ *              shared expert)
+ *   full       the stack as moe_ffn_forward takes it
+ *   slice      destination buffers (device, 16-byte aligned, written by the
+ *              call; the const of the struct's fields is not honoured here):
+ *              bf16: gate, up [n][Is][H], down [n][H][Is]; Int4: codes
+ *              gate, up [n][Is][H/2], down [n][H][Is/2] and scales gate, up
+ *              [n][Is][H/32], down [n][H][Is/32]
+ * Copies run asynchronously on `stream` (copy engine, no kernel).  Returns
+ * MOE_ERR_UNSUPPORTED unless I is a multiple of parts and Is a multiple of
+ * 64 (bf16) or 256 (Int4); MOE_ERR_INVALID_ARG for a part outside
+ * [0, parts), n_experts < 1 or null / misaligned pointers.
+ */
+moe_status moe_tp_slice_weights(const moe_dims* d, int32_t n_experts, int32_t part,
+                                int32_t parts, const moe_weights* full, const moe_weights* slice,
+                                moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the device status word that kernels using
  * this workspace have set (MOE_OK, or MOE_ERR_TIMEOUT when a bounded
  * device-side wait gave up), and clears it.
@@ -287,8 +348,10 @@ moe_status moe_debug_wait_timeout(void* ws, uint64_t budget_ns, moe_stream_t str
  * the CUDA cores.  T * E above MOE_STATIC_ROUTER_LOGITS returns
  * MOE_ERR_WORKSPACE before anything is launched.
  *
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * The first call in each device context looks up the array's device
+ * address (with that device current) and caches it under the context's
+ * unique id, so a device reset, which ends the context, leads to a fresh
+ * lookup; make the first call in a context before any stream capture.
  * All calls share the one array: calls that may overlap on the GPU (on
  * different streams, or from different threads, without ordering between
  * them) race on it and must be serialised by the caller.  The library

@@ -36,7 +36,8 @@ MOE_FLAG_ACCUMULATE = 2
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_size", "moe_router_topk",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
            "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout",
-           "moe_router_topk_static_scratch", "moe_dense_workspace_size", "moe_dense_ffn")
+           "moe_router_topk_static_scratch", "moe_dense_workspace_size", "moe_dense_ffn",
+           "moe_workspace_routing", "moe_tp_slice_weights")
 
 # T * E limit of moe_router_topk_static_scratch (floats of its fixed scratch)
 MOE_STATIC_ROUTER_LOGITS = 1 << 18
@@ -55,6 +56,12 @@ class MoeWeights(ctypes.Structure):
     _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
                 ("gate_scale", ctypes.c_void_p), ("up_scale", ctypes.c_void_p),
                 ("down_scale", ctypes.c_void_p)]
+
+
+class MoeRoutingView(ctypes.Structure):
+    _fields_ = [("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("gather", ctypes.c_void_p),
+                ("row_of", ctypes.c_void_p)]
 
 
 class MoeStageEvents(ctypes.Structure):
@@ -99,6 +106,8 @@ def lib() -> ctypes.CDLL:
                 "moe_router_topk_static_scratch": ([pd, vp, vp, vp, vp, vp, vp], i32),
                 "moe_dense_workspace_size": ([pd], sz),
                 "moe_dense_ffn": ([pd, vp, pw, vp, vp, sz, vp], i32),
+                "moe_workspace_routing": ([pd, vp, sz, ctypes.POINTER(MoeRoutingView)], i32),
+                "moe_tp_slice_weights": ([pd, i32, i32, i32, pw, pw, vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -227,3 +236,22 @@ def moe_dense_ffn(dims, x, weights: MoeWeights, out, ws, stream=None):
     _check(lib().moe_dense_ffn(ctypes.byref(dims), _ptr(x), ctypes.byref(weights), _ptr(out),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_dense_ffn")
+
+
+def moe_workspace_routing(dims, ws) -> MoeRoutingView:
+    """Device addresses of the routing a fused call left in ``ws`` (topk_idx,
+    topk_w, offsets, gather, row_of); see include/moe_ffn.h."""
+    view = MoeRoutingView()
+    _check(lib().moe_workspace_routing(ctypes.byref(dims), _ptr(ws),
+                                       ws.numel() * ws.element_size(), ctypes.byref(view)),
+           "moe_workspace_routing")
+    return view
+
+
+def moe_tp_slice_weights(dims, n_experts: int, part: int, parts: int, full: MoeWeights,
+                         slice_: MoeWeights, stream=None):
+    """Copies slice ``part`` of ``parts`` (along I) of a weight stack into the
+    buffers of ``slice_``; ``dims`` are the full layer's."""
+    _check(lib().moe_tp_slice_weights(ctypes.byref(dims), int(n_experts), int(part), int(parts),
+                                      ctypes.byref(full), ctypes.byref(slice_), _stream(stream)),
+           "moe_tp_slice_weights")

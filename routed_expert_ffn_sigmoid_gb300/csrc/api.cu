@@ -352,12 +352,19 @@ moe_status run_permute(const moe_dims& d, const int32_t* idx, const float* w, co
                        int32_t* offsets, int32_t* gather, int32_t* row_of, float* roww,
                        void* x_perm, int32_t* table, const Ws& ws, cudaStream_t s,
                        float* zero_out = nullptr, bool materialise = true) {
-  int32_t* blockcnt = ws.at<int32_t>(ws.L.blockcnt);
-  cudaError_t e = launch_perm_count(idx, d.T, d.E, d.top_k, blockcnt, s);
-  if (e == cudaSuccess)
-    e = launch_perm_scan(blockcnt, d.T, d.E, d.top_k, offsets, table, pick_bn(d.T), s);
-  if (e == cudaSuccess)
-    e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
+  cudaError_t e;
+  if (d.T <= kSmallT) {
+    // the one-CTA permutation the fused call runs at these sizes
+    const SmallPermOut p{nullptr, pick_bn(d.T), offsets, gather, row_of, roww, table, nullptr, 0};
+    e = launch_small_permutation(idx, w, d.T, d.E, d.top_k, p, s);
+  } else {
+    int32_t* blockcnt = ws.at<int32_t>(ws.L.blockcnt);
+    e = launch_perm_count(idx, d.T, d.E, d.top_k, blockcnt, s);
+    if (e == cudaSuccess)
+      e = launch_perm_scan(blockcnt, d.T, d.E, d.top_k, offsets, table, pick_bn(d.T), s);
+    if (e == cudaSuccess)
+      e = launch_perm_scatter(idx, w, blockcnt, d.T, d.E, d.top_k, gather, row_of, roww, s);
+  }
   if (e == cudaSuccess && materialise)
     e = launch_scatter_rows(static_cast<const uint16_t*>(x), row_of, d.T, d.H, d.top_k,
                             d.fmt == MOE_W_INT4_G32, static_cast<uint16_t*>(x_perm), zero_out,
@@ -914,6 +921,71 @@ moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* we
   return run_experts(dd, rows, table, weights, weights, kEpiScatterAdd, gather, roww, out, w, s);
 }
 
+moe_status moe_workspace_routing(const moe_dims* d, const void* ws, size_t ws_bytes,
+                                 moe_routing_view* view) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!view) return MOE_ERR_INVALID_ARG;
+  *view = moe_routing_view{};
+  if (d->T == 0) return MOE_OK;
+  Ws w;
+  if ((st = check_ws(*d, const_cast<void*>(ws), ws_bytes, &w)) != MOE_OK) return st;
+  view->topk_idx = w.at<const int32_t>(w.L.idx);
+  view->topk_w = w.at<const float>(w.L.w);
+  view->offsets = w.at<const int32_t>(w.L.offsets);
+  view->gather = w.at<const int32_t>(w.L.gather);
+  view->row_of = w.at<const int32_t>(w.L.row_of);
+  return MOE_OK;
+}
+
+moe_status moe_tp_slice_weights(const moe_dims* d, int32_t n_experts, int32_t part,
+                                int32_t parts, const moe_weights* full, const moe_weights* slice,
+                                moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (n_experts < 1 || parts < 1 || part < 0 || part >= parts) return MOE_ERR_INVALID_ARG;
+  if (d->I % parts != 0) return MOE_ERR_UNSUPPORTED;
+  const bool int4 = d->fmt == MOE_W_INT4_G32;
+  const size_t I = d->I, H = d->H, Is = I / parts, n = n_experts, p = part;
+  // each slice must itself be a valid intermediate size
+  if (Is % (int4 ? 256 : 64) != 0) return MOE_ERR_UNSUPPORTED;
+  if (!weights_ok(full, d->fmt) || !weights_ok(slice, d->fmt)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto dst = [](const void* q) { return const_cast<void*>(q); };
+  auto src = [](const void* q, size_t off) { return static_cast<const char*>(q) + off; };
+  // gate / up [n][I][K]: per expert, rows [p Is, (p+1) Is) are one
+  // contiguous run of `per_row` bytes per row
+  auto rows_slice = [&](const void* to, const void* from, size_t per_row) {
+    for (size_t e = 0; e < n; ++e) {
+      const size_t bytes = Is * per_row;
+      if (cudaMemcpyAsync(static_cast<char*>(dst(to)) + e * bytes,
+                          src(from, e * I * per_row + p * bytes), bytes,
+                          cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return false;
+    }
+    return true;
+  };
+  // down [n][H][K = I]: every one of the n H rows keeps the bytes of columns
+  // [p Is, (p+1) Is); `per_col` bytes per column (a fraction for codes)
+  auto cols_slice = [&](const void* to, const void* from, size_t full_row, size_t slice_row) {
+    return cudaMemcpy2DAsync(dst(to), slice_row, src(from, p * slice_row), full_row, slice_row,
+                             n * H, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  };
+  bool ok;
+  if (!int4) {
+    ok = rows_slice(slice->gate, full->gate, H * 2) && rows_slice(slice->up, full->up, H * 2) &&
+         cols_slice(slice->down, full->down, I * 2, Is * 2);
+  } else {
+    ok = rows_slice(slice->gate, full->gate, H / 2) && rows_slice(slice->up, full->up, H / 2) &&
+         rows_slice(slice->gate_scale, full->gate_scale, H / 32 * 2) &&
+         rows_slice(slice->up_scale, full->up_scale, H / 32 * 2) &&
+         cols_slice(slice->down, full->down, I / 2, Is / 2) &&
+         cols_slice(slice->down_scale, full->down_scale, I / 32 * 2, Is / 32 * 2);
+  }
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_workspace_status(void* ws, moe_stream_t stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -953,22 +1025,65 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_scratch_mu;
-float* g_static_scratch_addr[kMaxDevices] = {};
+struct StaticScratchAddr {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to
+  float* addr;
+};
+StaticScratchAddr g_static_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_static_router_logits on the current device, looked up
-// once per device (host code only sees a host-side stand-in for the symbol).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (never reused within the process, so a
+// device reset, which ends the context, also retires every address cached
+// for it).
+bool current_context_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  static const CtxGetIdFn get_id = []() -> CtxGetIdFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetIdFn>(p);
+  }();
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_static_router_logits in the current device's context
+// (host code only sees a host-side stand-in for the symbol).  Looked up with
+// that device current the first time a context uses it, then cached under
+// the context's id.
 moe_status static_scratch_for_current_device(float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  // no context may be current yet on this thread: the lookup binds the
+  // device's primary context, and the id is read after it
+  unsigned long long ctx_id = 0;
+  const bool have_id = current_context_id(&ctx_id);
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (!g_static_scratch_addr[dev]) {
+  StaticScratchAddr& c = g_static_scratch_addr[dev];
+  if (!have_id || !c.addr || c.ctx_id != ctx_id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_router_logits) != cudaSuccess || !p)
       return MOE_ERR_CUDA;
-    g_static_scratch_addr[dev] = static_cast<float*>(p);
+    if (!have_id && !current_context_id(&ctx_id)) return MOE_ERR_CUDA;
+    c.addr = static_cast<float*>(p);
+    c.ctx_id = ctx_id;
   }
-  *out = g_static_scratch_addr[dev];
+  *out = c.addr;
   return MOE_OK;
 }
 

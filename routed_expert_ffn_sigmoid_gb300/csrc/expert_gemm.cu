@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_kernels.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -100,27 +101,15 @@ __device__ __forceinline__ int n_entries_of(const int32_t* table, int dense_rows
 }
 
 __device__ __forceinline__ TileEntry entry_at(const int32_t* table, int dense_rows, int BN, int i) {
-  if (table) {
-    const int4 v = reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) +
-                                                 kTableHeaderBytes)[i];
-    return TileEntry{v.x, v.y, v.z, v.w};
-  }
+  if (table) return table_entry(table, i);
   return TileEntry{0, i * BN, min(BN, dense_rows - i * BN), 0};
 }
-
-__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 constexpr int kEpiThread0 = 64;  // first epilogue thread (warp 2)
 
 // Barrier among the four epilogue warps only.
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// silu(min(g, 10)) * clamp(u, -10, 10)
-__device__ __forceinline__ float clamped_swiglu(float g, float u) {
-  const float gc = fminf(g, 10.0f);
-  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
-  return gc / (1.0f + expf(-gc)) * uc;
-}
 
 struct SmemCarve {
   uint8_t* tiles;

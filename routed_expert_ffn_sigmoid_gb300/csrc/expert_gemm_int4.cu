@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_kernels.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -91,14 +92,6 @@ struct Int4Args {
   uint64_t budget_ns;
 };
 
-__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
-
-__device__ __forceinline__ float clamped_swiglu(float g, float u) {
-  const float gc = fminf(g, 10.0f);
-  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
-  return gc / (1.0f + expf(-gc)) * uc;
-}
-
 // One 32-bit word of codes (element i of the word in bits 4i .. 4i+3) -> its
 // eight fp16 weights (code - 8) * s as one 16-byte chunk, in the operand order
 // of an aligned 8-element group: (e0, e4), (e1, e5), (e2, e6), (e3, e7).  In
@@ -152,12 +145,6 @@ __device__ __forceinline__ void transpose4_lanes(float& x0, float& x1, float& x2
 
 __device__ __forceinline__ __half bf16_bits_to_half(uint32_t bits16) {
   return __float2half_rn(__uint_as_float(bits16 << 16));
-}
-
-__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int i) {
-  const int4 v =
-      reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + kTableHeaderBytes)[i];
-  return TileEntry{v.x, v.y, v.z, v.w};
 }
 
 template <int BN, int NA, int EPI>
@@ -243,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rph = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const TileEntry te = table_entry(a.table, tile / a.mblocks);
         const int mb = tile % a.mblocks;
         const bool sh = te.group == a.E;
         const int ge = sh ? 0 : te.group;
@@ -282,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bph = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const TileEntry te = table_entry(a.table, tile / a.mblocks);
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&b_empty[bs], bph ^ 1u, ab)) {
@@ -378,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t oph = 0, bph = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const TileEntry te = table_entry(a.table, tile / a.mblocks);
         const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ab)) break;
         tc_fence_after_sync();
@@ -427,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileEntry te = entry_at(a.table, tile / a.mblocks);
+      const TileEntry te = table_entry(a.table, tile / a.mblocks);
       const int mb = tile % a.mblocks;
       // Scatter-add: the tile's token ids and routing weights (nrows <= BN
       // <= 128), loaded while its MMAs run -- lane l holds rows l, l + 32,

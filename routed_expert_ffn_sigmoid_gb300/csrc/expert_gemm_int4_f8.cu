@@ -60,6 +60,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_kernels.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -119,18 +120,6 @@ struct F8Args {
   int* status;
   uint64_t budget_ns;
 };
-
-__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int i) {
-  const int4 v =
-      reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + kTableHeaderBytes)[i];
-  return TileEntry{v.x, v.y, v.z, v.w};
-}
-
-__device__ __forceinline__ float clamped_swiglu(float g, float u) {
-  const float gc = fminf(g, 10.0f);
-  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
-  return gc / (1.0f + expf(-gc)) * uc;
-}
 
 // Byte permute: bytes 0..3 of a, 4..7 of b, four 4-bit selectors in c[15:0].
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
@@ -310,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rph = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const TileEntry te = table_entry(a.table, tile / a.mblocks);
         const int mb = tile % a.mblocks;
         const bool sh = te.group == a.E;
         const int ge = sh ? 0 : te.group;
@@ -344,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bph = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.mblocks);
+        const TileEntry te = table_entry(a.table, tile / a.mblocks);
         for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait(&b_empty[bs], bph ^ 1u, ab)) {
             ok = false;
@@ -478,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t rph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const TileEntry te = entry_at(a.table, tile / a.mblocks);
+      const TileEntry te = table_entry(a.table, tile / a.mblocks);
       const int mb = tile % a.mblocks;
       const bool sh = te.group == a.E;
       const int f = mb * kBM + r;  // output feature (N_out % 128 == 0)

@@ -20,6 +20,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_kernels.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -74,18 +75,6 @@ struct TmArgs {
   int* status;
   uint64_t budget_ns;
 };
-
-__device__ __forceinline__ TileEntry entry_at(const int32_t* table, int i) {
-  const int4 v =
-      reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + kTableHeaderBytes)[i];
-  return TileEntry{v.x, v.y, v.z, v.w};
-}
-
-__device__ __forceinline__ float clamped_swiglu(float g, float u) {
-  const float gc = fminf(g, 10.0f);
-  const float uc = fminf(fmaxf(u, -10.0f), 10.0f);
-  return gc / (1.0f + expf(-gc)) * uc;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
@@ -160,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.nblocks);
+        const TileEntry te = table_entry(a.table, tile / a.nblocks);
         const int nb = tile % a.nblocks;
         const bool sh = te.group == a.E;
         const int ge = sh ? 0 : te.group;
@@ -243,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0, armed = 0, armed_par = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-          const TileEntry te = entry_at(a.table, tile / a.nblocks);
+          const TileEntry te = table_entry(a.table, tile / a.nblocks);
           for (int kb = 0; kb < KB; ++kb) {
             if (!mbar_wait(&a_empty[stage], phase ^ 1u, ab)) {
               ok = false;
@@ -286,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         --inflight;
       };
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileEntry te = entry_at(a.table, tile / a.nblocks);
+        const TileEntry te = table_entry(a.table, tile / a.nblocks);
         int tok[kBM / 4];  // token of row 4i + lane / 8
 #pragma unroll
         for (int i = 0; i < kBM / 4; ++i) {
@@ -335,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileEntry te = entry_at(a.table, tile / a.nblocks);
+      const TileEntry te = table_entry(a.table, tile / a.nblocks);
       const int nb = tile % a.nblocks;
       // this thread's token id and weight, loaded while the tile's MMAs run
       const int r = te.row0 + lrow;

@@ -9,8 +9,11 @@
 namespace moe {
 
 // Order-preserving map of a float onto uint32 (larger float -> larger key).
+// -0 and +0 compare equal as floats, so both map to the key of +0: a tie
+// between them is then decided by the expert index like any other tie.
 __device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float key_float(uint32_t k) {
@@ -100,13 +103,6 @@ __device__ __forceinline__ void warp0_exclusive_scan(int* v, int n, int* total) 
   if (lane == 0) *total = carry;
 }
 
-// Decode-size permutation by one CTA (T <= kSmallT tokens, any block size
-// that is a multiple of 32): from the top-k selection idx / w [T][k] in
-// global memory, the expert histogram, exclusive offsets (the shared expert
-// appended as group E), stable ranks from per-expert token bitmaps,
-// gather / row_of / row weights and the tile table -- the work of the count,
-// scan and scatter kernels with no launch in between.  The selection was
-// written by other CTAs of the calling grid: it is read past L1.
 __device__ __forceinline__ void write_tile_table(const int* off, int* ntile, int E, int BN,
                                                  int* n_entries, int32_t* __restrict__ table) {
   for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (off[g + 1] - off[g] + BN - 1) / BN;
@@ -128,6 +124,16 @@ __device__ __forceinline__ void write_tile_table(const int* off, int* ntile, int
   if (threadIdx.x == 0) table[0] = *n_entries;
 }
 
+// Decode-size permutation by one CTA (T <= kSmallT tokens, any block size
+// that is a multiple of 32): from the top-k selection idx / w [T][k] in
+// global memory, the expert histogram, exclusive offsets (the shared expert
+// appended as group E), stable ranks from per-expert token bitmaps,
+// gather / row_of / row weights and the tile table -- the work of the count,
+// scan and scatter kernels with no launch in between, with the same results.
+// The selection may have been written by other CTAs of the calling grid: it
+// is read past L1.  As in the multi-kernel path, an id outside [0, E) gets no
+// row (row_of = -1) and is left out of the counts; with w == nullptr no row
+// weights are written (roww may then be null too).
 __device__ __forceinline__ void small_permutation(const int32_t* idx, const float* w, int T, int E,
                                                   int k, int BN, int32_t* __restrict__ offsets,
                                                   int32_t* __restrict__ gather,
@@ -146,11 +152,12 @@ __device__ __forceinline__ void small_permutation(const int32_t* idx, const floa
   for (int i = threadIdx.x; i < E * (kSmallT / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     s_idx[i] = __ldcg(idx + i);
-    s_w[i] = __ldcg(w + i);
+    s_w[i] = w ? __ldcg(w + i) : 0.f;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     const int t = i / k, e = s_idx[i];
+    if (e < 0 || e >= E) continue;  // out-of-range ids are ignored
     atomicAdd(&cnt[e], 1);
     atomicOr(&bits[e][t >> 5], 1u << (t & 31));
   }
@@ -164,16 +171,20 @@ __device__ __forceinline__ void small_permutation(const int32_t* idx, const floa
   for (int g = threadIdx.x; g <= E + 1; g += blockDim.x) offsets[g] = cnt[g];
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     const int t = i / k, e = s_idx[i];
+    if (e < 0 || e >= E) {  // an out-of-range id gets no row
+      row_of[i] = -1;
+      continue;
+    }
     int rank = __popc(bits[e][t >> 5] & ((1u << (t & 31)) - 1u));
     for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bits[e][wd]);
     const int r = cnt[e] + rank;
     gather[r] = t;
     row_of[i] = r;
-    roww[r] = s_w[i];
+    if (w) roww[r] = s_w[i];
   }
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
     gather[k * T + t] = t;
-    roww[k * T + t] = 1.0f;
+    if (w) roww[k * T + t] = 1.0f;
   }
   write_tile_table(cnt, ntile, E, BN, &n_entries, table);
   if (table2) {

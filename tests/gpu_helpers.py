@@ -81,6 +81,21 @@ class DeviceLayer:
         assert st == moe.MOE_OK, moe.moe_status_string(st)
         return out.cpu().numpy()
 
+    def forward_with_routing(self, x_np: np.ndarray, flags: int = 0):
+        """moe_ffn_forward, plus the routing the call left in its workspace
+        (moe_workspace_routing): out, idx, w, offsets, gather, row_of."""
+        torch = torch_mod()
+        T = x_np.shape[0]
+        wl = self.wl
+        dims = moe.make_dims(T, wl.H, wl.E, wl.I, wl.I_shared, wl.top_k, wl.fmt, flags)
+        ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+        out = torch.full((T, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(dims, dev_u16(x_np), self.wr, self.b, self.exw, self.shw, out, ws)
+        st = moe.moe_workspace_status(ws)
+        assert st == moe.MOE_OK, moe.moe_status_string(st)
+        r = routing_arrays(dims, ws)
+        return (out.cpu().numpy(),) + r
+
     def router(self, x_np: np.ndarray):
         torch = torch_mod()
         T = x_np.shape[0]
@@ -119,3 +134,40 @@ def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, z_ref):
             e = int(idx_gpu[t, j])
             assert abs(w_gpu[t, j] - ref_by_e[e]) <= W_REL_TOL * ref_by_e[e] + 1e-7, \
                 f"token {t} e {e}: {w_gpu[t, j]} vs {ref_by_e[e]}"
+
+
+def routing_arrays(dims, ws):
+    """Copies of the routing a fused call left in the workspace tensor ws,
+    read at the addresses moe_workspace_routing gives: idx, w [T][k],
+    offsets [E+2], gather [(k+1)T], row_of [T][k]."""
+    torch = torch_mod()
+    v = moe.moe_workspace_routing(dims, ws)
+    T, k, E = dims.T, dims.top_k, dims.E
+    base = ws.data_ptr()
+
+    def take(addr, n, dtype):
+        off = addr - base
+        assert 0 <= off and off + 4 * n <= ws.numel()
+        return ws[off:off + 4 * n].view(dtype).cpu().numpy()
+
+    idx = take(v.topk_idx, T * k, torch.int32).reshape(T, k)
+    w = take(v.topk_w, T * k, torch.float32).reshape(T, k)
+    offsets = take(v.offsets, E + 2, torch.int32)
+    gather = take(v.gather, (k + 1) * T, torch.int32)
+    row_of = take(v.row_of, T * k, torch.int32).reshape(T, k)
+    return idx, w, offsets, gather, row_of
+
+
+def check_routing_bit_exact(idx, w, offsets, gather, row_of, z_ref, idx_ref, w_ref, E):
+    """The layer's own routing against the oracle: expert sets bit-exact
+    (slot order where the logits are clear, weights within W_REL_TOL), and
+    the permutation arrays equal to the oracle's permutation -- offsets and
+    gather depend only on the sets; row_of is compared with the oracle's
+    permutation of the same slot order."""
+    import oracle
+    compare_routing(idx, w, idx_ref, w_ref, z_ref)
+    r_off, r_gather, _ = oracle.permute(idx_ref, E)
+    assert np.array_equal(offsets, r_off)
+    assert np.array_equal(gather, r_gather)
+    _, _, r_row_of = oracle.permute(idx.astype(np.int32), E)
+    assert np.array_equal(row_of, r_row_of)

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 3
+    assert L.moe_abi_version() == 4
     for code in range(6):
         assert moe.moe_status_string(code).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)
@@ -108,6 +108,51 @@ def test_argument_errors_before_any_launch(L):
     d4 = moe.make_dims(8, 256, 288, 256, fmt="int4")
     assert _call_forward(d4, moe.moe_workspace_size(d4)) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_workspace_size(moe.make_dims(8, 256, 288, 64, fmt="int4")) == 0
+
+
+def test_routing_view_points_inside_the_workspace(L):
+    # pure address arithmetic: no device access, so it runs without a GPU
+    for T, fmt in ((1, "bf16"), (64, "int4"), (4096, "bf16")):
+        d = moe.make_dims(T, 4096, 288, 1536, fmt=fmt)
+        need = moe.moe_workspace_size(d)
+        base = 1 << 20
+        ws = _Fake(base, need)
+        v = moe.moe_workspace_routing(d, ws)
+        k, E = 8, 288
+        spans = [(v.topk_idx, T * k * 4), (v.topk_w, T * k * 4), (v.offsets, (E + 2) * 4),
+                 (v.gather, 9 * T * 4), (v.row_of, T * k * 4)]
+        for p, n in spans:
+            assert p % 16 == 0 and base + 256 <= p and p + n <= base + need
+        spans.sort()
+        for (p0, n0), (p1, _) in zip(spans, spans[1:]):
+            assert p0 + n0 <= p1  # disjoint
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_workspace_routing(d, _Fake(base, need - 1))
+        assert ei.value.code == moe.MOE_ERR_WORKSPACE
+    d0 = moe.make_dims(0, 4096, 288, 1536)
+    v0 = moe.moe_workspace_routing(d0, _Fake(0, 0))
+    assert v0.topk_idx is None and v0.row_of is None
+
+
+def test_tp_slice_rejects_bad_splits_before_any_copy(L):
+    w = moe.MoeWeights(0x30000, 0x40000, 0x50000, None, None, None)
+    full = moe.make_dims(8, 4096, 288, 1536)
+
+    def call(d, n, part, parts, src=w, dst=w):
+        return L.moe_tp_slice_weights(ctypes.byref(d), n, part, parts, ctypes.byref(src),
+                                      ctypes.byref(dst), None)
+
+    assert call(full, 288, 2, 2) == moe.MOE_ERR_INVALID_ARG       # part outside [0, parts)
+    assert call(full, 288, -1, 2) == moe.MOE_ERR_INVALID_ARG
+    assert call(full, 0, 0, 2) == moe.MOE_ERR_INVALID_ARG         # no experts
+    assert call(full, 288, 0, 0) == moe.MOE_ERR_INVALID_ARG
+    assert call(full, 288, 0, 5) == moe.MOE_ERR_UNSUPPORTED       # 1536 / 5 is not whole
+    assert call(full, 288, 0, 32) == moe.MOE_ERR_UNSUPPORTED      # 48 is not a multiple of 64
+    f4 = moe.make_dims(8, 4096, 288, 1536, fmt="int4")
+    assert call(f4, 288, 0, 4) == moe.MOE_ERR_UNSUPPORTED         # Int4 slices need 256s
+    assert call(f4, 288, 0, 2) == moe.MOE_ERR_INVALID_ARG         # Int4 needs scale pointers
+    odd = moe.MoeWeights(0x30001, 0x40000, 0x50000, None, None, None)
+    assert call(full, 288, 0, 2, dst=odd) == moe.MOE_ERR_INVALID_ARG  # misaligned
 
 
 def test_zero_tokens_is_a_no_op(L):

@@ -78,6 +78,37 @@ def test_exact_ties_go_to_the_lower_expert(T):
         assert rel_max_err(out, ref) <= TOL["bf16"]
 
 
+# T = 8: CUDA-core partial logits; T = 300: the tensor-core router
+@pytest.mark.parametrize("T", [8, 300])
+def test_signed_zero_logits_tie_to_the_lower_expert(T):
+    """x = 0 makes every logit its bias exactly.  Five experts lead clearly;
+    six have logit zero, the lower of each pair with bias -0.0 and router
+    weights of negative sign (so every product is -0 as well), the higher
+    with +0.0.  -0 and +0 are equal scores, so the last three slots go to
+    the three lowest of the six, whatever sign each kernel's sum ends with."""
+    wl = replace(TINY, T=T)
+    w_router, _ = synthetic.gen_router(wl)
+    w_router = w_router.copy()
+    b_router = np.full(wl.E, -5.0, np.float32)
+    lead = [2, 50, 90, 140, 200]
+    b_router[lead] = 5.0
+    neg_zero, pos_zero = [10, 30, 60], [11, 31, 61]
+    b_router[neg_zero] = np.float32(-0.0)
+    b_router[pos_zero] = np.float32(0.0)
+    w_router[neg_zero] |= np.uint16(0x8000)
+    w_router[pos_zero] &= np.uint16(0x7FFF)
+    x = np.zeros((T, wl.H), np.uint16)
+    idx, w = _route(wl, x, w_router, b_router, T)
+    want = np.array(sorted(lead + [10, 11, 30]), np.int32)
+    assert np.array_equal(np.sort(idx, axis=1), np.broadcast_to(want, idx.shape))
+    r_idx, r_w = oracle.topk(oracle.router_logits(x, w_router, b_router), wl.top_k)[:2]
+    assert np.array_equal(np.sort(r_idx, axis=1), np.sort(idx, axis=1))
+    for t in range(T):
+        ref_by_e = dict(zip(r_idx[t].tolist(), r_w[t].tolist()))
+        for j in range(wl.top_k):
+            assert abs(w[t, j] - ref_by_e[int(idx[t, j])]) <= 1e-6
+
+
 @pytest.mark.parametrize("T", [8, 300])
 def test_all_logits_tied_selects_the_first_experts(T):
     wl = replace(TINY, T=T)

@@ -15,7 +15,8 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU container
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import routed_expert_ffn_sigmoid_gb300 as moe  # noqa: E402
-from gpu_helpers import TOL, DeviceLayer, compare_routing, dev_u16, int4_operand_order  # noqa: E402,E501
+from gpu_helpers import (TOL, DeviceLayer, check_routing_bit_exact, compare_routing,  # noqa: E402
+                         dev_u16, int4_operand_order)
 
 
 @pytest.fixture(scope="module")
@@ -45,7 +46,7 @@ def test_forward_small_int4(small4):
     assert rel_max_err(out, _ref(small4, small4.inp.x)) <= TOL["int4"]
 
 
-@pytest.mark.parametrize("T", [1, 8, 64])
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
 def test_forward_decode_int4(decode4, T):
     x = decode4.inp.x[:T]
     out = decode4.forward(x)
@@ -106,11 +107,30 @@ def test_forward_skewed_prefill_int4_sampled(skewed4):
 
 
 def test_router_skewed_prefill(skewed4):
-    x = skewed4.inp.x[:2048]
+    x = skewed4.inp.x
     idx, w = skewed4.router(x)
     z = oracle.router_logits(x, skewed4.inp.w_router, skewed4.inp.b_router)
     ridx, rw, _ = oracle.topk(z, 8)
     compare_routing(idx, w, ridx, rw, z)
+
+
+def test_fused_routing_and_permutation_bit_exact_skewed(skewed4):
+    # all 16384 tokens: groups of up to ~16k rows under the Zipf load
+    x = skewed4.inp.x
+    _, idx, w, off, gather, row_of = skewed4.forward_with_routing(x)
+    z = oracle.router_logits(x, skewed4.inp.w_router, skewed4.inp.b_router)
+    ridx, rw, _ = oracle.topk(z, 8)
+    check_routing_bit_exact(idx, w, off, gather, row_of, z, ridx, rw, skewed4.wl.E)
+    assert np.diff(off).max() > 8000
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_fused_routing_and_permutation_bit_exact_decode_int4(decode4, T):
+    x = decode4.inp.x[:T]
+    _, idx, w, off, gather, row_of = decode4.forward_with_routing(x)
+    z = oracle.router_logits(x, decode4.inp.w_router, decode4.inp.b_router)
+    ridx, rw, _ = oracle.topk(z, 8)
+    check_routing_bit_exact(idx, w, off, gather, row_of, z, ridx, rw, decode4.wl.E)
 
 
 def test_int4_rejects_unaligned_shapes(small4):

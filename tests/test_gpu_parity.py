@@ -21,7 +21,8 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU container
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import routed_expert_ffn_sigmoid_gb300 as moe  # noqa: E402
-from gpu_helpers import TOL, DeviceLayer, compare_routing, dev_u16  # noqa: E402
+from gpu_helpers import (TOL, DeviceLayer, check_routing_bit_exact, compare_routing,  # noqa: E402
+                         dev_u16)
 
 
 # ------------------------------------------------------------------ fixtures
@@ -103,7 +104,9 @@ def _check_permute(layer, idx, x):
     assert np.array_equal(x_perm, x[r_gather])
 
 
-@pytest.mark.parametrize("T", [1, 64, 300])
+# 1 .. 128 tokens: the one-CTA permutation the fused call runs; 129 and
+# 300: the count / scan / scatter kernels
+@pytest.mark.parametrize("T", [1, 16, 17, 64, 128, 129, 300])
 def test_permute_decode_shapes(decode, T):
     x = decode.inp.x[:T] if T <= decode.wl.T else _gapped(decode, T)
     _, idx, _ = _ref_routing(decode, x)
@@ -257,6 +260,30 @@ def test_forward_forced_overflow_group(decode):
     ref, idx, _ = oracle.moe_forward(x[sample], inp.w_router, b, inp.experts, inp.shared, "bf16")
     assert all(sorted(r) == forced for r in idx.tolist())
     assert rel_max_err(out[sample], ref) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ the fused call's own routing
+
+# Up to 16 tokens the top-k kernel's last CTA permutes, up to 128 a one-CTA
+# launch, above that the count / scan / scatter kernels; 4096 tokens route
+# through the tensor-core logits.  The arrays compared are the ones the
+# call's grouped GEMMs consumed, read back from its workspace.
+@pytest.mark.parametrize("T", [1, 8, 16, 17, 64, 128, 129])
+def test_fused_routing_and_permutation_bit_exact_decode(decode, T):
+    x = decode.inp.x[:T] if T <= decode.wl.T else _gapped(decode, T)
+    out, idx, w, off, gather, row_of = decode.forward_with_routing(x)
+    z, ridx, rw = _ref_routing(decode, x)
+    check_routing_bit_exact(idx, w, off, gather, row_of, z, ridx, rw, decode.wl.E)
+    if T in (16, 17, 128, 129):  # sizes the other output tests do not run
+        sample = np.unique(np.concatenate([np.arange(0, T, 11), [T - 1]]))
+        assert rel_max_err(out[sample], _ref_forward(decode, x[sample])) <= TOL["bf16"]
+
+
+def test_fused_routing_and_permutation_bit_exact_prefill(prefill):
+    x = prefill.inp.x
+    _, idx, w, off, gather, row_of = prefill.forward_with_routing(x)
+    z, ridx, rw = _ref_routing(prefill, x)
+    check_routing_bit_exact(idx, w, off, gather, row_of, z, ridx, rw, prefill.wl.E)
 
 
 # ------------------------------------------------------------------ status / errors
