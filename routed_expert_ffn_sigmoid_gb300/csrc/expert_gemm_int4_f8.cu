@@ -36,28 +36,39 @@
 // 8 elements in the order (0, 1, 4, 5, 2, 3, 6, 7), the order the weight
 // bytes come out of e5m2_of_codes8.
 //
-// CTA = 15 warps, persistent over the flat tile list:
+// CTA = 16 warps, persistent over the flat tile list:
 //   warp 0, lane 0   code producer: TMA of the packed codes, 256 reduction
 //                    elements per raw stage
-//   warp 1           TMEM allocation; lane 0 issues tcgen05.mma kind::f8f6f4
-//                    (A e5m2, B e4m3)
+//   warps 1, 15      lane 0 of each issues tcgen05.mma kind::f8f6f4 (A e5m2
+//                    from TMEM, B e4m3 from shared memory): one matrix each
+//                    (gate/up) or two of a slot's scale groups each (down);
+//                    warp 1 also allocates TMEM
 //   warps 2..5       epilogue: per operand slot (four scale groups),
-//                    tcgen05.ld of their accumulators in two batches, scale
-//                    and add; after the last group the SwiGLU and the h
-//                    planes (gate/up) or the scatter-add / row store (down)
+//                    tcgen05.ld of the accumulator columns that hold tokens,
+//                    scale and add; after the last group the SwiGLU and the
+//                    h planes (gate/up) or the scatter-add / row store (down)
 //   warps 6..13      dequantisers, two threads per weight row (one per matrix
 //                    for gate/up, one per two of a slot's four groups for
-//                    down): code words -> e5m2 bytes (fp16 mask-and-or, one
-//                    half2 subtract, one byte permute per four codes), written
-//                    into the 128-byte-swizzled operand tile
-//   warp 14, lane 0  activation producer: TMA of the e4m3 planes
-// Accumulators: a ring of four-group entries over all 512 TMEM columns; the
-// MMA thread commits and the epilogue warps release one entry per operand
-// slot (a handshake every two groups cost ~12 % more: issuing the small MMAs
-// is what bounds these kernels).  Every wait is bounded as in the other GEMM
-// kernels.
+//                    down; a warp's rows are its TMEM lane quadrant): code
+//                    words -> e5m2 bytes (fp16 mask-and-or, one half2
+//                    subtract, one byte permute per four codes), stored into
+//                    the operand slot's TMEM columns (tcgen05.st)
+//   warp 14, lane 0  activation producer: TMA of the e4m3 planes, four
+//                    operand slots' B tiles per stage
+// TMEM holds the operand slots and a ring of accumulator entries, one entry
+// (four scale groups) per slot.  Per slot the issuers commit once each to the
+// entry's barrier; the epilogue waits on it, and so do the dequantisers
+// before they overwrite the slot's operand columns two slots later (the same
+// MMAs read them), which spares a commit per slot.  Why the operand is in
+// TMEM and the issue is split: measured on GB300, a 128 x 16 x 32 MMA costs
+// ~44 cycles to issue, tcgen05.st moves ~250 B per cycle per SM next to MMAs
+// without slowing them, and a commit costs ~200 cycles in this kernel; with
+// the operand in shared memory the kernel moved ~3 B of shared memory per
+// weight.  Every wait is bounded as in the other GEMM kernels.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "moe_kernels.h"
 #include "gemm_common.cuh"
@@ -71,20 +82,28 @@ constexpr int kSlotK = 128;                        // 8-bit elements per 128-byt
 constexpr int kRawK = 256;                         // reduction elements per raw stage
 constexpr int kSlotsPerRaw = kRawK / kSlotK;       // 2
 constexpr int kGroupsPerSlot = kSlotK / 32;        // 4
-constexpr int kATileBytes = kBM * kSlotK;          // 16 KB e5m2 operand per matrix
 constexpr int kCodeTileBytes = kBM * (kRawK / 2);  // 16 KB packed codes per matrix
 constexpr int kBRows = 16;
-constexpr int kBTileBytes = kBRows * kSlotK;       // 2 KB
-constexpr int kBStages = 8;
+constexpr int kBTileBytes = kBRows * kSlotK;       // 2 KB: one operand slot's B tile
+constexpr int kBSub = 4;                           // slots (B tiles) per B stage
+constexpr int kBStageBytes = kBSub * kBTileBytes;  // 8 KB
+constexpr int kBStages = 4;
 constexpr int kGroupsPerSync = 4;                  // groups per accumulator handshake (a slot)
 constexpr int kGroupsPerLoad = 2;                  // groups per TMEM load batch of the epilogue
 constexpr int kTmemCols = 512;
 constexpr int kBarBytes = 1024;
-constexpr int kThreads = 480;
+constexpr int kThreads = 512;
 constexpr int kDqThread0 = 192;
 constexpr int kDqThreads = 256;
 constexpr int kDqWarpEnd = 14;
 constexpr int kBWarp = 14;
+// The MMAs are issued by two threads on different SM sub-partitions (warps 1
+// and 15), each for one matrix (gate/up) or two of a slot's four scale
+// groups (down): a single issuer shares its sub-partition with two
+// dequantiser warps and loses issue slots to their ALU work (measured: 8
+// MMAs plus bookkeeping took ~1.6k cycles per slot, against ~0.4k alone).
+constexpr int kMmaWarp1 = 15;
+constexpr int kIssuers = 2;
 constexpr int kMaxGroups = 128;                    // K / 32 of the down projection (I <= 4096)
 
 template <int NA>
@@ -93,15 +112,23 @@ struct F8Cfg {
   static constexpr int kMaxTok = kBRows / kPlanes;            // 8 or 5
   static constexpr int kGroupCols = 16 * NA;                  // accumulator columns per group
   static constexpr int kEntryCols = kGroupsPerSync * kGroupCols;
-  static constexpr int kAccRing = kTmemCols / kEntryCols;     // 8 or 16
-  static constexpr int kSlotBytes = NA * kATileBytes;
-  static constexpr int kRawBytes = NA * kCodeTileBytes;
-  static constexpr int kRaw = NA == 2 ? 4 : 6;
+  // TMEM: the accumulator ring first, then the operand slots (A, e5m2:
+  // 128 lanes x 32 bytes = 8 columns per scale group and matrix)
   static constexpr int kSlots = NA == 2 ? 2 : 3;
-  static constexpr int kSmemBytes =
-      kSlots * kSlotBytes + kRaw * kRawBytes + kBStages * kBTileBytes + 1024 + kBarBytes;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static constexpr int kACols = NA * kGroupsPerSlot * 8;      // 64 or 32
+  static constexpr int kAccRing = (kTmemCols - kSlots * kACols) / kEntryCols;  // 3 or 6
+  static constexpr int kABase = kAccRing * kEntryCols;
+  static constexpr int kRawBytes = NA * kCodeTileBytes;
+  static constexpr int kRaw = NA == 2 ? 5 : 10;
+  static constexpr int kSmemBytes = kRaw * kRawBytes + kBStages * kBStageBytes + 1024 + kBarBytes;
+  static_assert(kSmemBytes <= 227 * 1024 - (NA == 1 ? 4 * kF8DownMaxRows * kMaxGroups * 4 : 0),
+                "shared memory");
+  static_assert(kABase + kSlots * kACols <= kTmemCols, "TMEM columns");
   static_assert(kMaxTok == (NA == 2 ? kF8MaxRows : kF8DownMaxRows), "tile entry rows");
+  // one accumulator entry per operand slot: the dequantisers reuse slot n's
+  // TMEM columns once acc_full of the entry of slot n - kSlots has completed
+  static_assert(kGroupsPerSync == kGroupsPerSlot, "one accumulator entry per slot");
+  static_assert(kSlots < kAccRing, "an entry is reused only after its slot's reuse");
 };
 
 struct F8Args {
@@ -155,24 +182,14 @@ __device__ __forceinline__ uint2 e5m2_of_codes8(uint32_t w) {
 // Position of element i (0..7) of an aligned group of 8 in that order.
 __device__ __forceinline__ int op_pos8(int i) { return (i & 1) | ((i & 2) << 1) | ((i & 4) >> 1); }
 
-__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// 32 TMEM lanes x 8 consecutive 32-bit columns (see tmem_ld_32x32b_x16).
-__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
+// D[tmem] = A[tmem] x B[smem]^T, kind::f8f6f4 (no accumulation into D: each
+// scale group has an accumulator of its own).  A: 128 lanes (rows) x K = 32
+// bytes in 8 consecutive columns, element k in byte k % 4 of column k / 4.
+__device__ __forceinline__ void umma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -182,6 +199,57 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float scale_of(const uint4& v, int g) {
   const uint32_t w = g < 2 ? v.x : g < 4 ? v.y : g < 6 ? v.z : v.w;
   return (g & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// 32 TMEM lanes x W consecutive 32-bit columns (W = 2, 4, 8 or 16; see
+// tmem_ld_32x32b_x16): the epilogue reads only the columns that hold tokens.
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+  if constexpr (W == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(taddr)
+                 : "memory");
+  } else if constexpr (W == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+  } else if constexpr (W == 8) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+  } else {
+    static_assert(W == 16, "column count");
+    tmem_ld_32x32b_x16(taddr, r);
+  }
+}
+
+// Gate/up epilogue, one TMEM load batch: the accumulators of kGroupsPerLoad
+// scale groups (gate at tq + 32 jj, up 16 columns further), W live columns
+// each, scaled by the groups' scales and added into acc0 (gate) / acc1 (up).
+template <int W>
+__device__ __forceinline__ void gateup_batch(uint32_t tq, const uint4& s0, const uint4& s1,
+                                             int gb, float (&acc0)[16], float (&acc1)[16]) {
+  uint32_t v[kGroupsPerLoad][2][W];
+#pragma unroll
+  for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+    tmem_ld_cols<W>(tq + jj * 32, v[jj][0]);
+    tmem_ld_cols<W>(tq + jj * 32 + 16, v[jj][1]);
+  }
+  tmem_ld_wait();
+#pragma unroll
+  for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+    const float sa = scale_of(s0, gb + jj), sb = scale_of(s1, gb + jj);
+#pragma unroll
+    for (int c = 0; c < W; ++c) {
+      acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
+      acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
+    }
+  }
 }
 
 // 4 x 4 transpose across the four lanes 4j .. 4j+3 of a warp: lane 4j+r
@@ -230,20 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // down: each epilogue warp's copy of its tile's h scales [token][group]
   __shared__ float s_hb[NA == 1 ? 4 : 1][NA == 1 ? kTok : 1][NA == 1 ? kMaxGroups : 1];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* slots = base;
-  uint8_t* raws = slots + Cfg::kSlots * Cfg::kSlotBytes;
+  uint8_t* raws = base;
   uint8_t* bring = raws + Cfg::kRaw * Cfg::kRawBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(bring + kBStages * kBTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bring + kBStages * kBStageBytes);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + Cfg::kRaw;
   uint64_t* b_full = raw_empty + Cfg::kRaw;
   uint64_t* b_empty = b_full + kBStages;
   uint64_t* a_full = b_empty + kBStages;
-  uint64_t* op_empty = a_full + Cfg::kSlots;
-  uint64_t* acc_full = op_empty + Cfg::kSlots;
+  uint64_t* acc_full = a_full + Cfg::kSlots;
   uint64_t* acc_empty = acc_full + Cfg::kAccRing;
-  uint64_t* drain = acc_empty + Cfg::kAccRing;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = acc_empty + Cfg::kAccRing;  // one per issuer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kIssuers);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,17 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_empty[i], kIssuers);
     }
-    for (int i = 0; i < Cfg::kSlots; ++i) {
-      mbar_init(&a_full[i], kDqThreads);
-      mbar_init(&op_empty[i], 1);
-    }
+    for (int i = 0; i < Cfg::kSlots; ++i) mbar_init(&a_full[i], kDqThreads);
     for (int i = 0; i < Cfg::kAccRing; ++i) {
-      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_full[i], kIssuers);
       mbar_init(&acc_empty[i], 128);
     }
-    mbar_init(drain, 1);
+    for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -288,8 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto code_tile = [&](int rs, int m) {
     return raws + rs * Cfg::kRawBytes + m * kCodeTileBytes;
   };
-  auto a_tile = [&](int os, int m) { return slots + os * Cfg::kSlotBytes + m * kATileBytes; };
-  auto b_tile = [&](int bs) { return bring + bs * kBTileBytes; };
+  // TMEM column of operand slot os, matrix m (lane 0)
+  auto a_col = [&](int os, int m) {
+    return static_cast<uint32_t>(Cfg::kABase + os * Cfg::kACols + m * kGroupsPerSlot * 8);
+  };
+  auto b_tile = [&](int bs, int sub) { return bring + bs * kBStageBytes + sub * kBTileBytes; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- code producer
@@ -334,15 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileEntry te = table_entry(a.table, tile / a.mblocks);
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int k0 = 0; k0 < KS; k0 += kBSub) {
+          const int nsub = min(kBSub, KS - k0);
           if (!mbar_wait(&b_empty[bs], bph ^ 1u, ab)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&b_full[bs], kBTileBytes);
+          mbar_arrive_expect_tx(&b_full[bs], nsub * kBTileBytes);
           armed |= 1u << bs;
           armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
-          tma_load_2d(b_tile(bs), &tm_b, &b_full[bs], ks * kSlotK, P * te.row0, pol);
+          for (int sub = 0; sub < nsub; ++sub)
+            tma_load_2d(b_tile(bs, sub), &tm_b, &b_full[bs], (k0 + sub) * kSlotK, P * te.row0,
+                        pol);
           if (++bs == kBStages) {
             bs = 0;
             bph ^= 1u;
@@ -354,48 +423,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6 && warp < kDqWarpEnd) {
     // ---------------------------------------------------------------- dequantisers
-    const int d = threadIdx.x - kDqThread0;
-    const int r = d & (kBM - 1);                // weight row of the tile
-    const int m = NA == 2 ? (d >> 7) : 0;       // gate/up: matrix
-    const int j0 = NA == 2 ? 0 : (d >> 7) * 2;  // down: first of two groups per slot
+    // a warp writes the TMEM lane quadrant (warp id % 4): row r of the tile
+    // is lane r; warps 6..9 take one matrix (or the first two groups of a
+    // slot), warps 10..13 the other
+    const int dw = (threadIdx.x - kDqThread0) >> 5;  // 0..7
+    const int r = (warp & 3) * 32 + lane;            // weight row of the tile = TMEM lane
+    const int m = NA == 2 ? (dw >> 2) : 0;           // gate/up: matrix
+    const int j0 = NA == 2 ? 0 : (dw >> 2) * 2;      // down: first of two groups per slot
     constexpr int kJ = NA == 2 ? kGroupsPerSlot : 2;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const int sw = r & 7;                       // 128-byte swizzle phase of this row
     int rs = 0, os = 0;
-    uint32_t rph = 0, oph = 0;
+    uint32_t rph = 0;
+    int n = 0;  // slots written so far (the MMA thread's accumulator entry n % kAccRing)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       for (int rb = 0; ok && rb < RB; ++rb) {
-        if (!mbar_wait(&raw_full[rs], rph, ab)) {
+        // warp-uniform waits: the TMEM stores below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[rs], rph, ab))) {
           ok = false;
           break;
         }
         const uint8_t* ct = code_tile(rs, m) + r * 128;
 #pragma unroll
         for (int sb = 0; sb < kSlotsPerRaw; ++sb) {
-          if (!mbar_wait(&op_empty[os], oph ^ 1u, ab)) {
-            ok = false;
-            break;
-          }
-          uint8_t* at = a_tile(os, m) + r * 128;
-          // code chunk 4 sb + j (32 codes, one scale group) -> operand chunks
-          // 2 j and 2 j + 1 (16 codes each)
+          // code chunk 4 sb + j (32 codes, one scale group) -> the group's 32
+          // e5m2 bytes, TMEM columns 8 j .. 8 j + 7 of this row's lane
+          uint32_t wv[kJ * 8];
 #pragma unroll
           for (int jj = 0; jj < kJ; ++jj) {
             const int j = j0 + jj;
             const uint4 cw = *reinterpret_cast<const uint4*>(ct + (((sb * 4 + j) ^ sw) << 4));
             const uint2 e0 = e5m2_of_codes8(cw.x), e1 = e5m2_of_codes8(cw.y);
             const uint2 e2 = e5m2_of_codes8(cw.z), e3 = e5m2_of_codes8(cw.w);
-            *reinterpret_cast<uint4*>(at + (((2 * j) ^ sw) << 4)) =
-                make_uint4(e0.x, e0.y, e1.x, e1.y);
-            *reinterpret_cast<uint4*>(at + (((2 * j + 1) ^ sw) << 4)) =
-                make_uint4(e2.x, e2.y, e3.x, e3.y);
+            wv[8 * jj + 0] = e0.x;
+            wv[8 * jj + 1] = e0.y;
+            wv[8 * jj + 2] = e1.x;
+            wv[8 * jj + 3] = e1.y;
+            wv[8 * jj + 4] = e2.x;
+            wv[8 * jj + 5] = e2.y;
+            wv[8 * jj + 6] = e3.x;
+            wv[8 * jj + 7] = e3.y;
           }
-          fence_proxy_async_smem();
+          // the MMAs of slot n - kSlots, the last to read these columns, have
+          // completed: the commit of their accumulator entry has arrived
+          if (n >= Cfg::kSlots) {
+            const int p = n - Cfg::kSlots;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[p % Cfg::kAccRing],
+                                                   (p / Cfg::kAccRing) & 1, ab))) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after_sync();
+          const uint32_t tcol = lane_base + a_col(os, m) + j0 * 8;
+          if constexpr (NA == 2)
+            tmem_st_32x32b_x32(tcol, wv);
+          else
+            tmem_st_32x32b_x16(tcol, wv);
+          tmem_st_wait();
+          tc_fence_before_sync();
           mbar_arrive(&a_full[os]);
-          if (++os == Cfg::kSlots) {
-            os = 0;
-            oph ^= 1u;
-          }
+          ++n;
+          if (++os == Cfg::kSlots) os = 0;
         }
         if (!ok) break;
         mbar_arrive(&raw_empty[rs]);
@@ -405,59 +495,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ---------------------------------------------------------------- MMA issuers
     if (lane == 0) {
+      const int mi = warp == 1 ? 0 : 1;  // issuer: matrix (gate/up) or group pair (down)
       // A e5m2 (format 1, bits 7..9), B e4m3 (format 0), fp32 accumulate
       const uint32_t idesc = idesc_f16(kBM, kBRows, false) | (1u << 7);
+      // gate/up: all four groups of matrix mi; down: groups 2 mi, 2 mi + 1
+      constexpr int kMyGroups = NA == 2 ? kGroupsPerSlot : kGroupsPerSlot / kIssuers;
+      const int g0 = NA == 2 ? 0 : mi * kMyGroups;
+      const uint32_t acc_off = NA == 2 ? mi * 16 : 0;  // gate / up accumulator of a group
       int os = 0, bs = 0, ring = 0;
       uint32_t oph = 0, bph = 0, rph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         for (int ks = 0; ks < KS; ++ks) {
-          if (!mbar_wait(&b_full[bs], bph, ab) || !mbar_wait(&a_full[os], oph, ab)) {
+          const int sub = ks % kBSub;
+          if ((sub == 0 && !mbar_wait(&b_full[bs], bph, ab)) || !mbar_wait(&a_full[os], oph, ab) ||
+              !mbar_wait(&acc_empty[ring], rph ^ 1u, ab)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(bs)));
-          const uint64_t d0 = sw128_kmajor_desc(smem_u32(a_tile(os, 0)));
-          const uint64_t d1 = sw128_kmajor_desc(smem_u32(a_tile(os, NA - 1)));
+          const uint64_t db = sw128_kmajor_desc(smem_u32(b_tile(bs, sub)));
+          const uint32_t ta = tmem_base + a_col(os, NA == 2 ? mi : 0);
+          const uint32_t dacc = tmem_base + ring * Cfg::kEntryCols + acc_off;
 #pragma unroll
-          for (int j0 = 0; j0 < kGroupsPerSlot; j0 += kGroupsPerSync) {
-            if (!mbar_wait(&acc_empty[ring], rph ^ 1u, ab)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-#pragma unroll
-            for (int jj = 0; jj < kGroupsPerSync; ++jj) {
-              const int j = j0 + jj;
-              const uint32_t dacc = tmem_base + ring * Cfg::kEntryCols + jj * Cfg::kGroupCols;
-              umma_f8(dacc, d0 + 2 * j, db + 2 * j, idesc, 0u);
-              if (NA == 2) umma_f8(dacc + 16, d1 + 2 * j, db + 2 * j, idesc, 0u);
-            }
-            umma_commit(&acc_full[ring]);
-            if (++ring == Cfg::kAccRing) {
-              ring = 0;
-              rph ^= 1u;
-            }
+          for (int jj = 0; jj < kMyGroups; ++jj) {
+            const int j = g0 + jj;
+            umma_f8_tmem_a(dacc + j * Cfg::kGroupCols, ta + 8 * j, db + 2 * j, idesc);
           }
-          if (!ok) break;
-          umma_commit(&op_empty[os]);
-          umma_commit(&b_empty[bs]);
+          umma_commit(&acc_full[ring]);
+          if (++ring == Cfg::kAccRing) {
+            ring = 0;
+            rph ^= 1u;
+          }
           if (++os == Cfg::kSlots) {
             os = 0;
             oph ^= 1u;
           }
-          if (++bs == kBStages) {
-            bs = 0;
-            bph ^= 1u;
+          if (sub == kBSub - 1 || ks == KS - 1) {  // the stage's last slot
+            umma_commit(&b_empty[bs]);
+            if (++bs == kBStages) {
+              bs = 0;
+              bph ^= 1u;
+            }
           }
         }
       }
-      umma_commit(drain);
-      mbar_wait_drain(drain, 0);
+      umma_commit(&drain[mi]);
+      mbar_wait_drain(&drain[mi], 0);
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
@@ -520,60 +607,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int gl = 0; gl < kGroupsPerSync; gl += kGroupsPerLoad) {
             const uint32_t tq = tq0 + gl * Cfg::kGroupCols;
             const int gb = gi + gl;  // first group of this load batch within the eight
-            if (NA == 2) {
-              if (2 * nt <= 8) {  // at most 4 tokens: columns 0..7 of each accumulator
-                uint32_t v[kGroupsPerLoad][2][8];
-#pragma unroll
-                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
-                  tmem_ld_32x32b_x8(tq + jj * 32, v[jj][0]);
-                  tmem_ld_32x32b_x8(tq + jj * 32 + 16, v[jj][1]);
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
-                  const float sa = scale_of(s0, gb + jj), sb = scale_of(s1, gb + jj);
-#pragma unroll
-                  for (int c = 0; c < 8; ++c) {
-                    acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
-                    acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
-                  }
-                }
-              } else {
-                uint32_t v[kGroupsPerLoad][2][16];
-#pragma unroll
-                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
-                  tmem_ld_32x32b_x16(tq + jj * 32, v[jj][0]);
-                  tmem_ld_32x32b_x16(tq + jj * 32 + 16, v[jj][1]);
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
-                  const float sa = scale_of(s0, gb + jj), sb = scale_of(s1, gb + jj);
-#pragma unroll
-                  for (int c = 0; c < 16; ++c) {
-                    acc0[c] = fmaf(sa, __uint_as_float(v[jj][0][c]), acc0[c]);
-                    acc1[c] = fmaf(sb, __uint_as_float(v[jj][1][c]), acc1[c]);
-                  }
-                }
-              }
+            if constexpr (NA == 2) {
+              // 2 nt live columns (hi and lo plane of each token)
+              if (nt == 1)
+                gateup_batch<2>(tq, s0, s1, gb, acc0, acc1);
+              else if (nt <= 2)
+                gateup_batch<4>(tq, s0, s1, gb, acc0, acc1);
+              else if (nt <= 4)
+                gateup_batch<8>(tq, s0, s1, gb, acc0, acc1);
+              else
+                gateup_batch<16>(tq, s0, s1, gb, acc0, acc1);
             } else {
-              uint32_t v[kGroupsPerLoad][16];
+              // 3 nt live columns (hi, mid and lo plane of each token)
+              auto down_batch = [&](auto wtag) {
+                constexpr int W = decltype(wtag)::value;
+                constexpr int kT = W == 16 ? kTok : W / 3;
+                uint32_t v[kGroupsPerLoad][W];
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerLoad; ++jj) tmem_ld_32x32b_x16(tq + jj * 16, v[jj]);
-              tmem_ld_wait();
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) tmem_ld_cols<W>(tq + jj * 16, v[jj]);
+                tmem_ld_wait();
 #pragma unroll
-              for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
-                const float sa = scale_of(s0, gb + jj);
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
+                  const float sa = scale_of(s0, gb + jj);
 #pragma unroll
-                for (int t = 0; t < kTok; ++t) {
-                  const float pv = (__uint_as_float(v[jj][3 * t]) +
-                                    __uint_as_float(v[jj][3 * t + 1])) +
-                                   __uint_as_float(v[jj][3 * t + 2]);
-                  const float hbv =
-                      s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gb + jj : 0];
-                  acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
+                  for (int t = 0; t < kT; ++t) {
+                    const float pv = (__uint_as_float(v[jj][3 * t]) +
+                                      __uint_as_float(v[jj][3 * t + 1])) +
+                                     __uint_as_float(v[jj][3 * t + 2]);
+                    const float hbv =
+                        s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gb + jj : 0];
+                    acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
+                  }
                 }
-              }
+              };
+              if (nt == 1)
+                down_batch(std::integral_constant<int, 4>{});
+              else if (nt <= 2)
+                down_batch(std::integral_constant<int, 8>{});
+              else
+                down_batch(std::integral_constant<int, 16>{});
             }
           }
           tc_fence_before_sync();
