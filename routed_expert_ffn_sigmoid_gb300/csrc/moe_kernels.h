@@ -56,6 +56,15 @@ struct SmallPermOut {
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
                                       int k, int32_t* idx, float* w, float* z,
                                       const SmallPermOut* perm, cudaStream_t s);
+// Routing of up to kRouteSmallT tokens (H <= 4096) in one launch: logits
+// (z [T][E], workspace), top-k (idx / w) and, in the last CTA to finish, the
+// permutation into `perm` (done: a counter that is zero before the launch
+// and zero again after it).  Also clears zero_n floats of zero_out.
+constexpr int kRouteSmallT = 16;
+cudaError_t launch_route_small(const uint16_t* x, const uint16_t* w_router, const float* b, int T,
+                               int H, int E, int k, float* z, int32_t* idx, float* w,
+                               const SmallPermOut& perm, float* zero_out, size_t zero_n,
+                               cudaStream_t s);
 // The same permutation as a one-CTA launch of its own (`done` unused).
 cudaError_t launch_small_permutation(const int32_t* idx, const float* w, int T, int E, int k,
                                      const SmallPermOut& p, cudaStream_t s);

@@ -27,38 +27,38 @@ constexpr int kTopkVPL = kMaxE / 32;  // logits held per lane
 // support with ROCmFP mix qtypes (105/106)", section "MoE FFN (REAL routed
 // expert execution)"; ties to the lower index: deterministic top-k, "feat(glm53):
 // add device-resident HIP backend for MI350P", "Key changes").
-// Lane L holds experts L, L+32, ...; each round takes the warp maximum of the
-// 64-bit key (score key << 32 | ~e): the larger score wins and an exact tie
+// Lane L holds experts L, L+32, ...  Each round, every lane takes its largest
+// remaining key (the first of equal keys: its lowest expert), the warp takes
+// the largest of those with one 32-bit max reduction, and the lowest expert
+// holding it with one min reduction: the larger score wins and an exact tie
 // goes to the lower expert index.  Lane j < k ends with slot j: *e_out, and
 // *w_out = sigmoid(z_j) / sum of the k sigmoids.  keys[i] = float_key(z) of
-// expert i * 32 + lane.
+// expert i * 32 + lane (any value where that expert does not exist).
 __device__ __forceinline__ void warp_topk_keys(const uint32_t (&keys)[kTopkVPL], int E, int k,
                                                int* e_out, float* w_out) {
   const int lane = threadIdx.x & 31;
+  const int nv = (E + 31) >> 5;  // key slots in use (warp-uniform)
   uint32_t taken = 0;
   int my_e = 0;
   float my_z = 0.f;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
+    uint32_t bk = 0;  // below every key of a float (float_key of -inf is 0x007FFFFF)
+    uint32_t be = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < kTopkVPL; ++i) {
+      if (i >= nv) break;
       const int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u)) {
-        const uint64_t key =
-            (static_cast<uint64_t>(keys[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
-        best = key > best ? key : best;
+      if (e < E && !((taken >> i) & 1u) && keys[i] > bk) {
+        bk = keys[i];
+        be = static_cast<uint32_t>(e);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e_win = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const int e_win = static_cast<int>(__reduce_min_sync(0xffffffffu, bk == mk ? be : 0xFFFFFFFFu));
     if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
     if (lane == j) {
       my_e = e_win;
-      my_z = key_float(static_cast<uint32_t>(best >> 32));
+      my_z = key_float(mk);
     }
   }
   const float s = lane < k ? 1.0f / (1.0f + expf(-my_z)) : 0.f;

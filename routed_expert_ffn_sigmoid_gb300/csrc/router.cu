@@ -308,6 +308,204 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ z, 
   }
 }
 
+
+// ---------------------------------------------------------------- one-launch routing, T <= 16
+// At decode sizes the routing is a chain of latencies, not of bytes (2.36 MB
+// of router weights): one launch does all of it.  CTA = 2 experts x 4 warps;
+// warp (e, q) covers quarter q of the reduction for expert e, every lane
+// issuing its router loads (and a batch of four tokens' x loads) before the
+// first use; the quarters are added in a fixed order with the bias, so the
+// logits are the same bits on every run.  The last CTA to finish (a counter
+// in the workspace, zero between calls) selects the top-k of every token,
+// one warp per token, and builds the permutation in shared memory: with at
+// most 16 x 16 (token, slot) pairs, counts and ranks are read off the pairs
+// directly, and one block-wide scan gives the tile table.
+
+constexpr int kRsExperts = 2;                           // experts per CTA
+constexpr int kRsSplit = 4;                             // warps per expert (reduction quarters)
+constexpr int kRsThreads = 32 * kRsExperts * kRsSplit;  // 256
+constexpr int kRsChunks = 4;                            // 16-byte chunks per lane (H <= 4096)
+constexpr int kRsTokBatch = 4;                          // tokens whose x loads are in flight together
+
+// Exclusive scan of v[0..n) in shared memory by the whole CTA (n <= 1024:
+// each warp scans 32-element chunks, warp 0 scans the chunk sums); *total
+// gets the sum.  Every thread calls it; it synchronises before it returns.
+__device__ __forceinline__ void block_exclusive_scan(int* v, int n, int* total) {
+  __shared__ int chunk_sum[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int nchunks = (n + 31) >> 5;
+  for (int c = warp; c < nchunks; c += nw) {
+    const int i = c * 32 + lane;
+    const int x = i < n ? v[i] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (i < n) v[i] = incl - x;
+    if (lane == 31) chunk_sum[c] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < nchunks ? chunk_sum[lane] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane < nchunks) chunk_sum[lane] = incl - x;
+    if (lane == 31) *total = incl;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) v[i] += chunk_sum[i >> 5];
+  __syncthreads();
+}
+
+// Tile table of groups 0..E (counts from the offsets off[0..E+1]): entries
+// of at most BN rows, in group order.
+__device__ __forceinline__ void small_tile_table(const int* off, int* ntile, int E, int BN,
+                                                 int32_t* __restrict__ table) {
+  __shared__ int n_entries;
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) ntile[g] = (off[g + 1] - off[g] + BN - 1) / BN;
+  __syncthreads();
+  block_exclusive_scan(ntile, E + 1, &n_entries);
+  TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(table) + kTableHeaderBytes);
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) {
+    const int o = off[g], c = off[g + 1] - o;
+    for (int i = 0, r = 0; r < c; ++i, r += BN) {
+      TileEntry te;
+      te.group = g;
+      te.row0 = o + r;
+      te.nrows = min(BN, c - r);
+      te.pad = 0;
+      ent[ntile[g] + i] = te;
+    }
+  }
+  if (threadIdx.x == 0) table[0] = n_entries;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kRsThreads) route_small_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ b,
+    int T, int H, int E, int k, float* __restrict__ z, int32_t* __restrict__ idx,
+    float* __restrict__ w, const SmallPermOut perm, float4* __restrict__ zero_out,
+    size_t zero_n4) {
+  __shared__ float red[kRsExperts][kRsSplit][kRouteSmallT];
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();  // dependents wait for this grid's completion themselves
+  clear_grid(zero_out, zero_n4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int el = warp / kRsSplit, q = warp % kRsSplit;
+  const int e = blockIdx.x * kRsExperts + el;
+  const int cq = H / (8 * kRsSplit);  // 16-byte chunks per quarter (H % 128 == 0)
+  if (e < E) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e) * H) + q * cq;
+    uint4 wv[kRsChunks];
+#pragma unroll
+    for (int i = 0; i < kRsChunks; ++i) {
+      const int c = lane + 32 * i;
+      wv[i] = c < cq ? __ldg(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int t0 = 0; t0 < T; t0 += kRsTokBatch) {
+      uint4 xv[kRsTokBatch][kRsChunks];
+#pragma unroll
+      for (int tt = 0; tt < kRsTokBatch; ++tt) {
+        const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + tt) * H) + q * cq;
+#pragma unroll
+        for (int i = 0; i < kRsChunks; ++i) {
+          const int c = lane + 32 * i;
+          xv[tt][i] = (t0 + tt < T && c < cq) ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kRsTokBatch; ++tt) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRsChunks; ++i) {
+          float xf[8], wf[8];
+          bf16x8_to_f32(xv[tt][i], xf);
+          bf16x8_to_f32(wv[i], wf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc = fmaf(xf[j], wf[j], acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0 && t0 + tt < T) red[el][q][t0 + tt] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kRsExperts * kRouteSmallT) {
+    const int e2 = blockIdx.x * kRsExperts + threadIdx.x / kRouteSmallT;
+    const int t = threadIdx.x % kRouteSmallT;
+    const int l2 = threadIdx.x / kRouteSmallT;
+    if (e2 < E && t < T)
+      z[static_cast<size_t>(t) * E + e2] =
+          ((red[l2][0][t] + red[l2][1][t]) + (red[l2][2][t] + red[l2][3][t])) + b[e2];
+  }
+  // the last CTA to finish selects and permutes
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(perm.done, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ int s_e[kRouteSmallT * kMaxTopK];
+  __shared__ float s_w[kRouteSmallT * kMaxTopK];
+  __shared__ int s_off[kMaxE + 2];
+  __shared__ int s_nt[kMaxE + 1];
+  __shared__ int s_total;
+  const int P = T * k;
+  for (int t = warp; t < T; t += kRsThreads / 32) {
+    uint32_t keys[kTopkVPL];
+    const float* zr = z + static_cast<size_t>(t) * E;
+#pragma unroll
+    for (int i = 0; i < kTopkVPL; ++i) {
+      const int ee = i * 32 + lane;
+      keys[i] = ee < E ? float_key(__ldcg(zr + ee)) : 0u;
+    }
+    int ew;
+    float wv;
+    warp_topk_keys(keys, E, k, &ew, &wv);
+    if (lane < k) {
+      s_e[t * k + lane] = ew;
+      s_w[t * k + lane] = wv;
+      idx[static_cast<size_t>(t) * k + lane] = ew;
+      w[static_cast<size_t>(t) * k + lane] = wv;
+    }
+  }
+  for (int g = threadIdx.x; g <= E; g += kRsThreads) s_off[g] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += kRsThreads) atomicAdd(&s_off[s_e[p]], 1);
+  if (threadIdx.x == 0) s_off[E] = T;  // the shared expert: every token
+  __syncthreads();
+  block_exclusive_scan(s_off, E + 1, &s_total);
+  if (threadIdx.x == 0) s_off[E + 1] = s_total;
+  __syncthreads();
+  for (int g = threadIdx.x; g <= E + 1; g += kRsThreads) perm.offsets[g] = s_off[g];
+  // rank of a pair among the earlier pairs of its expert (a token's ids are
+  // distinct, so earlier pairs of an expert belong to earlier tokens)
+  for (int p = threadIdx.x; p < P; p += kRsThreads) {
+    const int ee = s_e[p];
+    int rank = 0;
+    for (int p2 = 0; p2 < p; ++p2) rank += s_e[p2] == ee;
+    const int r = s_off[ee] + rank, t = p / k;
+    perm.gather[r] = t;
+    perm.row_of[p] = r;
+    perm.roww[r] = s_w[p];
+  }
+  for (int t = threadIdx.x; t < T; t += kRsThreads) {
+    perm.gather[P + t] = t;
+    perm.roww[P + t] = 1.0f;
+  }
+  small_tile_table(s_off, s_nt, E, perm.BN, perm.table);
+  if (perm.table2) small_tile_table(s_off, s_nt, E, perm.BN2, perm.table2);
+  if (threadIdx.x == 0) *perm.done = 0;
+}
 }  // namespace
 
 cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* w_router, const float* b,
@@ -334,6 +532,18 @@ cudaError_t launch_router_partials(const uint16_t* x, const uint16_t* w_router, 
   const dim3 grid((E + kPartExperts - 1) / kPartExperts, router_slices(H));
   return launch_pdl(router_partial_kernel, grid, dim3(kPartThreads), kPartSmem, s, x, w_router,
                     T, H, E, part, reinterpret_cast<float4*>(zero_out), zero_n / 4);
+}
+
+cudaError_t launch_route_small(const uint16_t* x, const uint16_t* w_router, const float* b, int T,
+                               int H, int E, int k, float* z, int32_t* idx, float* w,
+                               const SmallPermOut& perm, float* zero_out, size_t zero_n,
+                               cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (T > kRouteSmallT || H > kRsChunks * 32 * 8 * kRsSplit || !perm.done)
+    return cudaErrorInvalidValue;
+  return launch_pdl(route_small_kernel, dim3((E + kRsExperts - 1) / kRsExperts), dim3(kRsThreads),
+                    0, s, x, w_router, b, T, H, E, k, z, idx, w, perm,
+                    reinterpret_cast<float4*>(zero_out), zero_n / 4);
 }
 
 cudaError_t launch_router_reduce_topk(const float* part, const float* b, int T, int H, int E,
