@@ -102,7 +102,7 @@ __device__ __forceinline__ int n_entries_of(const int32_t* table, int dense_rows
 
 __device__ __forceinline__ TileEntry entry_at(const int32_t* table, int dense_rows, int BN, int i) {
   if (table) return table_entry(table, i);
-  return TileEntry{0, i * BN, min(BN, dense_rows - i * BN), 0};
+  return TileEntry{0, i * BN, min(BN, dense_rows - i * BN), (dense_rows + BN - 1) / BN};
 }
 
 constexpr int kEpiThread0 = 64;  // first epilogue thread (warp 2)

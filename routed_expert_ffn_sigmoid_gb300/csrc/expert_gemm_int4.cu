@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- raw producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      // codes read by one token tile stream through L2 (evict_first); those
+      // of a group cut into several token tiles (heavy experts, the shared
+      // expert) are read again by its other tiles
+      const uint64_t pol_once = policy_evict_first(), pol_again = policy_evict_last();
       int rs = 0;
       uint32_t rph = 0, armed = 0, armed_par = 0;
       bool ok = true;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mb = tile % a.mblocks;
         const bool sh = te.group == a.E;
         const int ge = sh ? 0 : te.group;
+        const uint64_t pol = te.ntiles > 1 ? pol_again : pol_once;
         for (int rb = 0; rb < RB; ++rb) {
           if (!mbar_wait(&raw_empty[rs], rph ^ 1u, ab)) {
             ok = false;
@@ -264,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kBWarp) {
     // ---------------------------------------------------------------- activation producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
+      // activation rows: read by the mblocks tiles of their entry, which run
+      // at about the same time; at prefill they exceed L2 (9 T K 2 bytes)
+      const uint64_t pol = policy_evict_normal();
       int bs = 0;
       uint32_t bph = 0, armed = 0, armed_par = 0;
       bool ok = true;
@@ -410,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
+    // the scatter-add's output lines receive one addition per (token, slot)
+    // spread over the launch: kept resident in L2 between them
+    const uint64_t pol_out = policy_evict_last();
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -465,10 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 0xffffffffu, j == 0 ? tw[0] : j == 1 ? tw[1] : j == 2 ? tw[2] : tw[3], src);
             const int c = cb + r4;
             if (c < te.nrows && f < a.N_out) {
-              if (t >= 0) {
-                atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(t) * a.N_out),
-                          make_float4(wr * x0, wr * x1, wr * x2, wr * x3));
-              }
+              if (t >= 0)
+                red_add_f32x4(ob + static_cast<size_t>(t) * a.N_out,
+                              make_float4(wr * x0, wr * x1, wr * x2, wr * x3), pol_out);
             }
           }
         } else if (f < a.N_out) {

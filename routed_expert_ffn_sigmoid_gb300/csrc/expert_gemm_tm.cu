@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- weight producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // weights read by one token tile stream through L2 (evict_first);
+      // those of a group cut into several token tiles (the shared expert at
+      // prefill, heavy experts) are read again by its other tiles
+      const uint64_t pol_w = policy_evict_first(), pol_wr = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
@@ -162,10 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&b_full[stage], Cfg::kBStageBytes);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &b_full[stage], kb * kBK, nb * FN, ge, pol_w);
+          const uint64_t pw = te.ntiles > 1 ? pol_wr : pol_w;
+          tma_load_3d(sb, sh ? &tm_sb0 : &tm_b0, &b_full[stage], kb * kBK, nb * FN, ge, pw);
           if (NBM == 2)
             tma_load_3d(sb + Cfg::kBTileBytes, sh ? &tm_sb1 : &tm_b1, &b_full[stage], kb * kBK,
-                        nb * FN, ge, pol_w);
+                        nb * FN, ge, pw);
           if (++stage == Cfg::kBStages) {
             stage = 0;
             phase ^= 1u;
@@ -227,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!gat) {
       // ---------------------------------------------------------------- token producer (TMA)
       if (lane == 0) {
-        const uint64_t pol_x = policy_evict_last();
+        // token planes: read by the nblocks tiles of their entry, which run
+        // at about the same time; at prefill they exceed L2 (h is 9 T I 4
+        // bytes), so they are not kept past that
+        const uint64_t pol_x = policy_evict_normal();
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_par = 0;
         bool ok = true;
@@ -321,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int q = warp & 3;
     const int lrow = q * 32 + lane;  // token row of the tile this thread owns
+    // the scatter-add's output lines receive one addition per (token, slot)
+    // spread over the launch: kept resident in L2 between them
+    const uint64_t pol_out = policy_evict_last();
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -367,13 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           pl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           pl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         } else if (EPI == kEpiScatterAdd) {
-          float4* po = reinterpret_cast<float4*>(a.out + static_cast<size_t>(t) * a.N_out + f);
+          float* po = a.out + static_cast<size_t>(t) * a.N_out + f;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            atomicAdd(po + i, make_float4(wr * __uint_as_float(v0[4 * i]),
-                                          wr * __uint_as_float(v0[4 * i + 1]),
-                                          wr * __uint_as_float(v0[4 * i + 2]),
-                                          wr * __uint_as_float(v0[4 * i + 3])));
+            red_add_f32x4(po + 4 * i,
+                          make_float4(wr * __uint_as_float(v0[4 * i]),
+                                      wr * __uint_as_float(v0[4 * i + 1]),
+                                      wr * __uint_as_float(v0[4 * i + 2]),
+                                      wr * __uint_as_float(v0[4 * i + 3])),
+                          pol_out);
         } else {
           float4* po = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * a.N_out + f);
 #pragma unroll

@@ -18,8 +18,10 @@ constexpr int kSmallThreads = 512;
 
 // One grouped-GEMM work entry: rows [row0, row0 + nrows) of group `group`
 // (group == E is the shared expert).  nrows <= the launch's token tile BN.
+// ntiles: the number of entries of the group, so that a kernel knows
+// whether other tiles will read the same weights (L2 policy).
 struct TileEntry {
-  int32_t group, row0, nrows, pad;
+  int32_t group, row0, nrows, ntiles;
 };
 
 // ---------------------------------------------------------------- router

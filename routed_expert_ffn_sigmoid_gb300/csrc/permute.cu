@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
       te.group = g;
       te.row0 = off[g] + r;
       te.nrows = min(BN, c - r);
-      te.pad = 0;
+      te.ntiles = (c + BN - 1) / BN;
       ent[ntile[g] + i] = te;
     }
   }
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(1024) table_from_offsets_kernel(const int32_t*
       te.group = g;
       te.row0 = o + r;
       te.nrows = min(BN, c - r);
-      te.pad = 0;
+      te.ntiles = (c + BN - 1) / BN;
       ent[ntile[g] + i] = te;
     }
   }
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(256) dense_rows_kernel(int T, int BN, int32_t*
       te.group = 0;
       te.row0 = i * BN;
       te.nrows = min(BN, T - i * BN);
-      te.pad = 0;
+      te.ntiles = n;
       ent[i] = te;
     }
   }

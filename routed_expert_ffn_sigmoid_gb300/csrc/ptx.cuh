@@ -180,6 +180,21 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// out[0..3] += v, one 16-byte reduction in L2 under an L2 eviction policy
+// (the fp32 output of the scatter-add receives one such addition per
+// (token, slot) at different times of a launch: evict_last keeps its lines
+// resident between them).
+__device__ __forceinline__ void red_add_f32x4(float* out, float4 v, uint64_t policy) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(out),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 

@@ -117,7 +117,7 @@ __device__ __forceinline__ void write_tile_table(const int* off, int* ntile, int
       te.group = g;
       te.row0 = o + r;
       te.nrows = min(BN, c - r);
-      te.pad = 0;
+      te.ntiles = (c + BN - 1) / BN;
       ent[ntile[g] + i] = te;
     }
   }
