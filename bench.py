@@ -10,7 +10,11 @@ seeded x batches are cycled so the routed experts differ step to step, and
 L2 is flushed (a 512 MB write) before every timed step; only the layer call
 itself sits between the step's CUDA events.
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle, the
+Prints one JSON line (rank 0).  At N = 1 it also carries a per_config block:
+every workload's configurations (decode bf16 / Int4 at 1, 8, 32 and 64
+tokens, prefill bf16 at 4096, skewed Int4 prefill at 16384), each timed the
+same way with its own clock record, roofline and oracle rate
+(--no-per-config skips it).  --impl reference times the CPU oracle, the
 plain implementation written from the method's description, on the host
 cores, on a bounded sample of the same workload.
 
