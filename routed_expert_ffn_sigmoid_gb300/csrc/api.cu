@@ -392,7 +392,8 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
                        const int32_t* gather, const float* roww, float* out, const Ws& ws,
                        cudaStream_t s, const moe_stage_events* ev = nullptr,
                        const int32_t* xrows = nullptr, float* zero_out = nullptr,
-                       const float* xinv = nullptr, const int32_t* down_table = nullptr) {
+                       const float* xinv = nullptr, const int32_t* down_table = nullptr,
+                       const void* x_shared_first = nullptr) {
   const int rows = rows_of(d);
   const int nsm = sm_count();
   if (d.fmt == MOE_W_INT4_G32 && xinv && down_table) {
@@ -596,6 +597,17 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
   G.table = table;
   G.xrows = xrows;
   G.BN = BN;
+  // fused layer: the shared expert's tiles (rows = the tokens in order) run
+  // before the kernel waits for the routing, reading x directly
+  if (x_shared_first && d.top_k > 0) {
+    if (!encode_kmajor(&G.tm_xs, x_shared_first, bf16, d.H, d.T, 1, 16)) return MOE_ERR_CUDA;
+    G.n_sh = (d.T + BN - 1) / BN;
+    G.T = d.T;
+    G.sh_row0 = d.top_k * d.T;
+  } else {
+    G.tm_xs = G.tm_x;
+    G.n_sh = 0;
+  }
   G.K = d.H;
   G.I = d.I;
   G.E = d.E;
@@ -753,11 +765,11 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   const int32_t* xrows = rows_from_x ? gather : nullptr;
   if (!det)
     return run_experts(*d, rows_src, table, experts, shared, kEpiScatterAdd, gather, roww, out, w,
-                       s, ev, xrows, zero_gemm, xinv, table2);
+                       s, ev, xrows, zero_gemm, xinv, table2, x);
   // deterministic: unweighted rows, then the fixed-order combination
   float* y_perm = w.at<float>(L.y_perm);
   if ((st = run_experts(*d, rows_src, table, experts, shared, kEpiStoreRows, nullptr, nullptr,
-                        y_perm, w, s, ev, xrows, zero_gemm, xinv, table2)) != MOE_OK)
+                        y_perm, w, s, ev, xrows, zero_gemm, xinv, table2, x)) != MOE_OK)
     return st;
   const cudaError_t e = launch_combine(y_perm, w.at<int32_t>(L.row_of), wts, d->T, d->H,
                                        d->top_k, accumulate, out, s);

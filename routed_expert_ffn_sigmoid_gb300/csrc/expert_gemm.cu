@@ -74,6 +74,10 @@ struct GateUpArgs {
   const int32_t* table;
   const int32_t* xrows;  // non-null: token rows gathered from x by xrows[r] (tm_x over x)
   int K, I, E, a_rows, total_rows;
+  // > 0: the shared expert's first: its n_sh = ceil(T / BN) entries (rows
+  // sh_row0 + t, token rows x[t] through tm_xs) lead the unit order and are
+  // computed before the wait on the routing; the table's routed entries follow
+  int n_sh, T, sh_row0;
   int ksplit;            // units per tile along K (1: no split)
   float* partial;        // ksplit > 1: fp32 partial G/U per unit
   int* counters;         // ksplit > 1: finished units per tile (zero between calls)
@@ -162,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_up,
                   const __grid_constant__ CUtensorMap tm_sgate,
                   const __grid_constant__ CUtensorMap tm_sup,
-                  const __grid_constant__ CUtensorMap tm_x, const GateUpArgs a) {
+                  const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_xs, const GateUpArgs a) {
   using Cfg = GateUpCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const SmemCarve sm = carve(smem_raw, Cfg::kStages, Cfg::kStageBytes);
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_sgate);
     tma_prefetch_desc(&tm_sup);
     tma_prefetch_desc(&tm_x);
+    if (a.n_sh) tma_prefetch_desc(&tm_xs);
   }
   if (warp == 1) {
     tmem_alloc(sm.tmem_holder, Cfg::kTmemCols);
@@ -186,12 +192,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *sm.tmem_holder;
   const AbortState ab{sm.abort_flag, a.status, a.budget_ns};
 
-  pdl_wait();
   pdl_launch_dependents();
   const int mblocks = (a.I + kBM - 1) / kBM;
-  const int total = n_entries_of(a.table, 0, BN) * mblocks;
-  const int units = total * a.ksplit;
   const int KB = a.K / kBK;
+  // The shared expert's units need nothing the routing writes (its rows are
+  // the tokens in order, read from x), so each role runs them before it
+  // waits for the preceding kernels; the rest of the unit list comes from
+  // the table after that wait.  Every role walks the same unit sequence.
+  const int units_sh = a.n_sh * mblocks * a.ksplit;
+  auto entry_of = [&](int i) -> TileEntry {
+    if (i < a.n_sh)
+      return TileEntry{a.E, a.sh_row0 + i * BN, min(BN, a.T - i * BN), a.n_sh};
+    return entry_at(a.table, 0, BN, i - a.n_sh);
+  };
+  auto all_units = [&]() { return n_entries_of(a.table, 0, BN) * mblocks * a.ksplit; };
+  // units this role may process so far; a role past them waits, then reads
+  // the table (the routed entries plus the shared ones it already ran)
+  auto advance = [&](int u, int& units, bool& waited) {
+    if (u < units) return true;
+    if (waited) return false;
+    pdl_wait();
+    waited = true;
+    units = all_units();
+    return u < units;
+  };
 
   if (warp == 0) {
     // Producer warp.  Lane 0 waits for a free stage, arms it and loads the
@@ -212,22 +236,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the weight stream keeps its copies in flight.
       TileEntry te_next{};
       int tok_next[4] = {0, 0, 0, 0};
+      int fetched = -1;  // unit whose entry / rows te_next, tok_next hold
       auto fetch_unit = [&](int uu) {
-        te_next = entry_at(a.table, 0, BN, (uu / a.ksplit) / mblocks);
-        if (gat && lane < (te_next.nrows + 3) / 4) {
+        const int ei = (uu / a.ksplit) / mblocks;
+        te_next = entry_of(ei);
+        if (gat && ei >= a.n_sh && lane < (te_next.nrows + 3) / 4) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tok_next[j] = a.xrows[te_next.row0 + min(4 * lane + j, te_next.nrows - 1)];
         }
+        fetched = uu;
       };
-      if (blockIdx.x < units) fetch_unit(blockIdx.x);
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int units = a.n_sh ? units_sh : 0;
+      bool waited = false;
+      for (int u = blockIdx.x; ok && advance(u, units, waited); u += gridDim.x) {
+        if (fetched != u) fetch_unit(u);
         const int tile = u / a.ksplit, sp = u % a.ksplit;
         const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
         const TileEntry te = te_next;
         // gathered rows of this lane (rows past the group repeat its last row)
         const int tok[4] = {tok_next[0], tok_next[1], tok_next[2], tok_next[3]};
+        // the next unit's entry ahead of time, while it needs no wait
         if (u + static_cast<int>(gridDim.x) < units) fetch_unit(u + gridDim.x);
+        const bool shared_early = (tile / mblocks) < a.n_sh;  // rows straight from x (tm_xs)
         const int mb = tile % mblocks;
         const bool sh = te.group == a.E;
         const CUtensorMap* mg = sh ? &tm_sgate : &tm_gate;
@@ -235,9 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ge = sh ? 0 : te.group;
         const int nchunks = (te.nrows + kChunkRows - 1) / kChunkRows;
         const int ngather = (te.nrows + 3) / 4;  // gather4 loads of the tile (gathered rows)
+        const bool gat_u = gat && !shared_early;
         const uint32_t bytes = 2u * a.a_rows * kRowBytes +
-                               (gat ? ngather * 4 * kRowBytes : nchunks * kChunkBytes);
-        const bool issuer = gat && lane < ngather;
+                               (gat_u ? ngather * 4 * kRowBytes : nchunks * kChunkBytes);
+        const bool issuer = gat_u && lane < ngather;
         for (int kb = kb0; kb < kb1; ++kb) {
           uint8_t* st = sm.tiles + stage * Cfg::kStageBytes;
           bool go = true;
@@ -249,7 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
               tma_load_3d(st, mg, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
               tma_load_3d(st + kATileBytes, mu, &sm.full[stage], kb * kBK, mb * kBM, ge, pol_w);
-              if (!gat)
+              if (shared_early)
+                for (int c = 0; c < nchunks; ++c)
+                  tma_load_2d(st + 2 * kATileBytes + c * kChunkBytes, &tm_xs, &sm.full[stage],
+                              kb * kBK, te.row0 - a.sh_row0 + c * kChunkRows, pol_x);
+              else if (!gat)
                 for (int c = 0; c < nchunks; ++c)
                   tma_load_2d(st + 2 * kATileBytes + c * kChunkBytes, &tm_x, &sm.full[stage],
                               kb * kBK, te.row0 + c * kChunkRows, pol_x);
@@ -280,10 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      int units = a.n_sh ? units_sh : 0;
+      bool waited = false;
+      for (int u = blockIdx.x; ok && advance(u, units, waited); u += gridDim.x) {
         const int tile = u / a.ksplit, sp = u % a.ksplit;
         const int kb0 = sp * KB / a.ksplit, kb1 = (sp + 1) * KB / a.ksplit;
-        const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+        const TileEntry te = entry_of(tile / mblocks);
         const uint32_t idesc = idesc0 | (static_cast<uint32_t>(round16(te.nrows) >> 3) << 17);
         if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, ab)) break;
         tc_fence_after_sync();
@@ -328,9 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    int units = a.n_sh ? units_sh : 0;
+    bool waited = false;
+    for (int u = blockIdx.x; advance(u, units, waited); u += gridDim.x) {
       const int tile = u / a.ksplit;
-      const TileEntry te = entry_at(a.table, 0, BN, tile / mblocks);
+      const TileEntry te = entry_of(tile / mblocks);
       const int mb = tile % mblocks;
       if (a.ksplit > 1) {
         // Split along K: this unit's partial G and U go to global memory; the
@@ -667,8 +707,10 @@ cudaError_t gateup_dispatch(const GateUpLaunch& L, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  GateUpArgs a{L.table, L.xrows, L.K, L.I, L.E, L.a_rows, L.total_rows, L.ksplit > 0 ? L.ksplit : 1,
-               L.partial, L.counters, L.h0, L.h1, L.status, L.budget_ns};
+  GateUpArgs a{L.table,      L.xrows,  L.K,  L.I,          L.E,
+               L.a_rows,     L.total_rows, L.n_sh, L.T, L.sh_row0,
+               L.ksplit > 0 ? L.ksplit : 1, L.partial, L.counters, L.h0, L.h1, L.status,
+               L.budget_ns};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
   cfg.blockDim = dim3(kThreads);
@@ -679,7 +721,8 @@ cudaError_t gateup_dispatch(const GateUpLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L.tm_gate, L.tm_up, L.tm_sgate, L.tm_sup, L.tm_x, a);
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_gate, L.tm_up, L.tm_sgate, L.tm_sup, L.tm_x,
+                            L.tm_xs, a);
 }
 
 template <int BN, int NB, bool kBf16, int EPI>

@@ -118,6 +118,11 @@ cudaError_t launch_combine(const float* y_perm, const int32_t* row_of, const flo
 
 struct GateUpLaunch {
   CUtensorMap tm_gate, tm_up, tm_sgate, tm_sup, tm_x;
+  // shared expert first (fused layer): n_sh > 0 entries of the shared group
+  // (rows sh_row0 + t, tokens x[t] through tm_xs: x [T][K], 16-row boxes)
+  // run before the kernel waits for the routing
+  CUtensorMap tm_xs;
+  int n_sh, T, sh_row0;
   const int32_t* table;
   const int32_t* xrows;  // null: tm_x maps x_perm (16-row boxes); else tm_x maps x
                          // (1-row boxes) and row r of the tile is x[xrows[r]]
