@@ -45,8 +45,9 @@ int pick_bn(int T) {
   return 128;
 }
 
-// Int4 weights up to 64 tokens: gate/up on 8-bit operands (entries of at
-// most kF8MaxRows rows), down on the fp16 path over the same entries.
+// Int4 weights up to 64 tokens: gate/up and down both on 8-bit operands
+// (gate/up entries of at most kF8MaxRows rows, down entries of at most
+// kF8DownMaxRows rows in a table of their own).
 bool int4_f8(const moe_dims& d) {
   return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0 && d.I <= 4096;
 }
