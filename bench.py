@@ -93,14 +93,23 @@ def gateup_bytes(wl, distinct):
     return w + rows * wl.H * 2 + h
 
 
-def gateup_traffic_per_launch(wl, units):
-    """DRAM bytes of one gate/up launch from the committed ncu capture
-    (profiles/gateup_traffic.json), scaled by the expert units processed;
-    None when the kernel source changed since the capture, the workload
-    shape differs, or the launch runs another kernel (above 64 tokens the
-    token-major kernel serves gate/up)."""
+def down_bytes(wl, distinct):
+    """Down projection: down weights of distinct experts + shared, h rows read
+    (two bf16 planes, or one fp16 plane), out written once (fp32)."""
+    rows = (wl.top_k + 1) * wl.T
+    w = (distinct + 1) * (wl.I * wl.H) * (2 if wl.fmt == "bf16" else 0.5 + 2 / 32)
+    return w + rows * wl.I * (4 if wl.fmt == "bf16" else 2) + wl.T * wl.H * 4
+
+
+def traffic_per_launch(wl, units, record="gateup_traffic.json"):
+    """DRAM bytes of one launch of the kernel a committed ncu capture covers
+    (profiles/<record>: gateup_traffic.json for the gate/up kernel,
+    decode_ffn_traffic.json for the one-launch decode FFN), scaled by the
+    expert units processed; None when the record is absent, the kernel source
+    changed since the capture, the workload shape differs, or the launch runs
+    another kernel (above 64 tokens the token-major kernels serve)."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+    p = os.path.join(ROOT, "profiles", record)
     if (not os.path.exists(p) or wl.fmt != "bf16" or (wl.H, wl.I) != (4096, 1536)
             or wl.T > 64):
         return None
@@ -230,7 +239,7 @@ def dist_env():
     return rank, world, local
 
 
-def config_of(wl, world, args=None):
+def config_of(wl, world, args=None, one_launch=False):
     modes = []
     if args is not None and args.deterministic:
         modes.append("deterministic combination")
@@ -249,7 +258,9 @@ def config_of(wl, world, args=None):
             "stage_split": ("events between the stages of each call" if args is not None
                             and args.eager else
                             "second pass of K replays of graphs with event nodes between the "
-                            "stages (gate/up duration for the roofline)"),
+                            "stages (gate/up duration for the roofline)")
+                           + ("; gate/up and down are one launch (the gate/up stage holds both)"
+                              if one_launch else ""),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -442,8 +453,14 @@ def run_ours(args, wl, rank, world, local):
 
     hbm_peak, tc_peak, tc_sust, peak_src = peaks()
     mean_distinct = sum(distinct[s % N_BATCHES] for s in range(args.steps)) / args.steps
+    # the dominant kernel: gate/up, or with one launch gate/up + down together
+    # (the timed call's gate/up stage then brackets both projections)
+    one_launch = moe.moe_ffn_one_launch(dims) == 1
     gu_ms = statistics.mean(stage_ms[2])
-    gu_bytes = statistics.mean(gateup_bytes(wl, distinct[s % N_BATCHES]) for s in range(args.steps))
+    gu_bytes = statistics.mean(
+        gateup_bytes(wl, distinct[s % N_BATCHES])
+        + (down_bytes(wl, distinct[s % N_BATCHES]) if one_launch else 0)
+        for s in range(args.steps))
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9
     layer_bytes = statistics.mean(algorithmic_bytes(wl, distinct[s % N_BATCHES])
                                   for s in range(args.steps))
@@ -468,11 +485,15 @@ def run_ours(args, wl, rank, world, local):
                       "after the MMA, fp32 accumulate" if wl.T <= 64 else
                       "int4 weights dequantised to fp16, fp32 accumulate"),
             "data": "synthetic (seeded generator; random-init weights)",
-            "config": config_of(wl, world, args),
-            "roofline": {"bound": "hbm", "kernel": "gateup_swiglu (tcgen05 grouped gate/up)",
+            "config": config_of(wl, world, args, one_launch),
+            "roofline": {"bound": "hbm",
+                         "kernel": ("decode_ffn (tcgen05 gate/up + down, one launch)" if one_launch
+                                    else "gateup_swiglu (tcgen05 grouped gate/up)"),
                          "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
-                         "traffic": gateup_traffic_per_launch(wl, mean_distinct + 1),
+                         "traffic": (traffic_per_launch(wl, mean_distinct + 1,
+                                                        "decode_ffn_traffic.json") if one_launch
+                                     else traffic_per_launch(wl, mean_distinct + 1)),
                          "peak_source": f"{peak_src} hbm_gbs",
                          "algorithmic_bytes_per_launch": gu_bytes, "mean_launch_ms": gu_ms},
             "layer": {"algorithmic_GBps": layer_gbs, "hbm_frac": layer_gbs / hbm_peak,
@@ -484,7 +505,8 @@ def run_ours(args, wl, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
             # T <= 128: logits, one-CTA routing, gather, gate/up, down; larger T:
-            "gpu_launches": layer_launches(wl.T, args.deterministic, wl.fmt) * args.steps,
+            "gpu_launches": (layer_launches(wl.T, args.deterministic, wl.fmt)
+                             - (1 if one_launch else 0)) * args.steps,
             "clocks": clk.summary(),
         }
         if (world == 1 and not args.no_per_config and not args.deterministic
@@ -609,7 +631,8 @@ def time_config(moe, dev, wl, layer, host_x, w_router_np, b_router_np, experts_n
             "ms_p10": float(np.percentile(step_ms, 10)), "ms_p90": float(np.percentile(step_ms, 90)),
             "value": wl.T / (ms / 1e3), "unit": "tokens/s", "GBps": gbs, "TFLOPps": tflops,
             "distinct_experts_mean": mean_distinct, "roofline": roof,
-            "gpu_launches": layer_launches(wl.T, False, wl.fmt) * steps,
+            "gpu_launches": (layer_launches(wl.T, False, wl.fmt)
+                             - (1 if moe.moe_ffn_one_launch(dims) == 1 else 0)) * steps,
             "clocks": clk.summary(), "cpu_baseline": cpu}
 
 

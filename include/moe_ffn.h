@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 4
+#define MOE_FFN_ABI_VERSION 5
 
 /* A cudaStream_t, spelled without the CUDA headers. */
 typedef struct CUstream_st* moe_stream_t;
@@ -313,6 +313,18 @@ moe_status moe_workspace_routing(const moe_dims* d, const void* ws, size_t ws_by
 moe_status moe_tp_slice_weights(const moe_dims* d, int32_t n_experts, int32_t part,
                                 int32_t parts, const moe_weights* full, const moe_weights* slice,
                                 moe_stream_t stream);
+
+/*
+ * How moe_ffn_forward runs the expert FFN for these dims: 1 when gate/up and
+ * down are one kernel launch (bf16 weights, up to 64 tokens, H a multiple of
+ * 256, I of 128, not MOE_FLAG_DETERMINISTIC: a persistent kernel in which
+ * each down unit waits, through counters in the workspace, for the gate/up
+ * tiles of its expert group), 0 when they are two launches, -1 for invalid
+ * dims.  For profilers and benchmarks: with one launch the gate/up stage of
+ * moe_ffn_forward_timed brackets both projections and the down stage is
+ * empty.  Host-only; launches nothing.
+ */
+int moe_ffn_one_launch(const moe_dims* d);
 
 /*
  * Synchronises `stream`, returns the device status word that kernels using

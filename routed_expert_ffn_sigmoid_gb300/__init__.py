@@ -37,7 +37,7 @@ EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_size", "moe_ro
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
            "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout",
            "moe_router_topk_static_scratch", "moe_dense_workspace_size", "moe_dense_ffn",
-           "moe_workspace_routing", "moe_tp_slice_weights")
+           "moe_workspace_routing", "moe_tp_slice_weights", "moe_ffn_one_launch")
 
 # T * E limit of moe_router_topk_static_scratch (floats of its fixed scratch)
 MOE_STATIC_ROUTER_LOGITS = 1 << 18
@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
                 "moe_dense_ffn": ([pd, vp, pw, vp, vp, sz, vp], i32),
                 "moe_workspace_routing": ([pd, vp, sz, ctypes.POINTER(MoeRoutingView)], i32),
                 "moe_tp_slice_weights": ([pd, i32, i32, i32, pw, pw, vp], i32),
+                "moe_ffn_one_launch": ([pd], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -236,6 +237,12 @@ def moe_dense_ffn(dims, x, weights: MoeWeights, out, ws, stream=None):
     _check(lib().moe_dense_ffn(ctypes.byref(dims), _ptr(x), ctypes.byref(weights), _ptr(out),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_dense_ffn")
+
+
+def moe_ffn_one_launch(dims) -> int:
+    """1 when moe_ffn_forward runs gate/up and down as one launch for these
+    dims, 0 for two launches, -1 for invalid dims (include/moe_ffn.h)."""
+    return int(lib().moe_ffn_one_launch(ctypes.byref(dims)))
 
 
 def moe_workspace_routing(dims, ws) -> MoeRoutingView:

@@ -30,6 +30,8 @@ struct Layout {
       hinv, y_perm;
   size_t partial, counters;
   size_t partial_units;  // K-split units the partial buffer holds (0: no split possible)
+  size_t ready;          // one-launch decode FFN: counters per entry, then finished CTAs
+  int n_ready;           // entries the ready counters cover (0: no one-launch FFN)
   size_t total;
 };
 
@@ -64,6 +66,24 @@ size_t table_bytes(const moe_dims& d) {
 
 constexpr int kMaxSplit = 8;
 constexpr int kSplitTileLimit = 1024;  // tile counts from which no split is considered
+
+// Upper bound on the tile-table entries of a layer call: at most one entry
+// per row and per (group, BN rows).
+int entries_bound(const moe_dims& d) {
+  const int rows = rows_of(d);
+  const int BN = pick_bn(d.T);
+  return std::min((d.E + 1) + (rows + BN - 1) / BN, rows);
+}
+
+// The fused bf16 layer call runs gate/up and down as one persistent launch
+// (decode_ffn_kernel) for weights-as-M tiles up to this many tokens.
+constexpr int kOneLaunchFfnMaxTokens = 64;
+
+bool one_launch_ffn(const moe_dims& d) {
+  return d.fmt == MOE_W_BF16 && d.top_k > 0 && d.T <= kOneLaunchFfnMaxTokens &&
+         pick_bn(d.T) <= 64 && d.I % 128 == 0 && d.H % 256 == 0 &&
+         !(d.flags & MOE_FLAG_DETERMINISTIC);
+}
 
 // Upper bound on the gate/up tiles of the weight-rows-as-M kernels: at most
 // one entry per row and per (group, BN rows).
@@ -125,6 +145,8 @@ Layout layout_of(const moe_dims& d) {
   L.partial_units = tiles < kSplitTileLimit ? static_cast<size_t>(tiles) * kMaxSplit : 0;
   L.partial = take(L.partial_units * 2 * pick_bn(d.T) * 128 * 4);
   L.counters = take(L.partial_units ? static_cast<size_t>(tiles) * 4 : 0);
+  L.n_ready = one_launch_ffn(d) ? entries_bound(d) : 0;
+  L.ready = take(L.n_ready ? static_cast<size_t>(L.n_ready + 2) * 4 : 0);
   L.total = o;
   return L;
 }
@@ -629,10 +651,14 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     const long units = static_cast<long>(tiles) * S;
     G.grid = units < nsm ? static_cast<int>(units) : nsm;
   }
-  record(ev, 2, s);
-  cudaError_t e = launch_gateup(G, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  record(ev, 3, s);
+  // the fused layer call: gate/up and down as one persistent launch
+  const bool one_launch = x_shared_first && G.n_sh > 0 && epilogue == kEpiScatterAdd &&
+                          ws.L.n_ready > 0 && one_launch_ffn(d);
+  if (!one_launch) {
+    record(ev, 2, s);
+    if (launch_gateup(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(ev, 3, s);
+  }
 
   DownLaunch D{};
   if (!encode_weights(&D.tm_a, ex->down, bf16, d.I, d.H, d.E) ||
@@ -669,7 +695,33 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     const long units = tiles * D.ksplit;
     D.grid = units < nsm ? static_cast<int>(units) : nsm;
   }
-  e = launch_down(D, s);
+  if (one_launch) {
+    FfnLaunch F{};
+    F.g = G;
+    F.tm_down = D.tm_a;
+    F.tm_sdown = D.tm_a_shared;
+    F.tm_h0 = D.tm_b0;
+    F.tm_h1 = D.tm_b1;
+    // down units of 256 output features (two row blocks against one h tile)
+    F.ks_d = split_for(static_cast<long>(std::min(max_entries, rows)) * (d.H / 256), d.I / 64, nsm);
+    F.ready = ws.at<int>(ws.L.ready);
+    F.n_ready = ws.L.n_ready;
+    F.gather = gather;
+    F.roww = roww;
+    F.out = out;
+    F.out_rows = d.T;
+    // one CTA per SM at most: the units wait on one another across CTAs
+    const long units = static_cast<long>(ws.L.n_ready) *
+                       ((d.I / 128) * G.ksplit + (d.H / 256) * F.ks_d);
+    F.grid = units < nsm ? static_cast<int>(units) : nsm;
+    // one kernel: the gate/up stage event brackets it, the down stage is empty
+    record(ev, 2, s);
+    const cudaError_t e = launch_decode_ffn(F, s);
+    record(ev, 3, s);
+    record(ev, 4, s);
+    return from_cuda(e);
+  }
+  const cudaError_t e = launch_down(D, s);
   record(ev, 4, s);
   return from_cuda(e);
 }
@@ -942,6 +994,11 @@ moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* we
   // one contribution per output element: the atomic add onto zero (or onto
   // the caller's values) gives the same bits on every run
   return run_experts(dd, rows, table, weights, weights, kEpiScatterAdd, gather, roww, out, w, s);
+}
+
+int moe_ffn_one_launch(const moe_dims* d) {
+  if (check_dims(d) != MOE_OK) return -1;
+  return one_launch_ffn(*d) ? 1 : 0;
 }
 
 moe_status moe_workspace_routing(const moe_dims* d, const void* ws, size_t ws_bytes,

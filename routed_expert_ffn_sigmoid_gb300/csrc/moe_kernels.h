@@ -146,6 +146,29 @@ cudaError_t launch_gateup(const GateUpLaunch& L, cudaStream_t s);
 
 enum DownEpilogue : int { kEpiScatterAdd = 0, kEpiStoreRows = 1, kEpiRouter = 2 };
 
+// The decode FFN of a fused layer call in one persistent launch (bf16
+// weights, weights-as-M tiles of BN <= 64 token rows, scatter-add output):
+// every gate/up unit, then every down unit, with per-entry counters in
+// place of the kernel boundary.  g describes the gate/up half (n_sh > 0:
+// the shared expert's entries come first); the down half reads h through
+// tm_h0 / tm_h1 (16-row boxes) and the down weights through tm_down /
+// tm_sdown.  ready: n_ready + 2 ints (per-entry counters, finished CTAs,
+// the unit queue's counter), zero before the launch and zero again after it.  grid must not exceed the SM count (the units wait on one
+// another across CTAs).
+struct FfnLaunch {
+  struct GateUpLaunch g;
+  CUtensorMap tm_down, tm_sdown, tm_h0, tm_h1;
+  int ks_d;          // K-split units per down tile (1 = none)
+  int* ready;
+  int n_ready;
+  const int32_t* gather;
+  const float* roww;
+  float* out;        // [T][H], added into
+  int out_rows;
+  int grid;
+};
+cudaError_t launch_decode_ffn(const FfnLaunch& L, cudaStream_t s);
+
 struct DownLaunch {
   CUtensorMap tm_a, tm_a_shared, tm_b0, tm_b1;
   const int32_t* table;  // null: dense tiles over `dense_rows` rows, group 0

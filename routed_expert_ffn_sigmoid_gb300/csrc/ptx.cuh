@@ -103,6 +103,45 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// ------------------------------------------------------------ counters in global memory
+// (signals between the CTAs of one persistent launch)
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (TMA) accesses: a TMA load issued after it sees data that the
+// thread acquired through a generic load before it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until the counter *p, raised by other CTAs of the launch, reaches
+// `target`.  Bounded like mbar_wait: false when the CTA is aborting or the
+// budget ran out (the abort is then raised).
+__device__ __forceinline__ bool wait_counter(const int* p, int target, const AbortState& a) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((n & 15u) == 0) {
+      if (*a.flag) return false;
+      if (globaltimer_ns() - t0 > a.budget_ns) {
+        raise_abort(a);
+        return false;
+      }
+    }
+  }
+}
+
 // A wait bounded by a fixed budget only (used while draining after an abort).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();

@@ -69,11 +69,14 @@ class DeviceLayer:
         return torch.zeros(moe.moe_workspace_size(self.dims(T)), dtype=torch.uint8,
                            device="cuda")
 
-    def forward(self, x_np: np.ndarray):
+    def forward(self, x_np: np.ndarray, ws=None):
+        """moe_ffn_forward on a fresh zeroed workspace, or on `ws` (a workspace
+        of dims(T) that earlier calls used)."""
         torch = torch_mod()
         T = x_np.shape[0]
         dims = self.dims(T)
-        ws = self.workspace(T)
+        if ws is None:
+            ws = self.workspace(T)
         x = dev_u16(x_np)
         out = torch.empty((T, self.wl.H), dtype=torch.float32, device="cuda")
         moe.moe_ffn_forward(dims, x, self.wr, self.b, self.exw, self.shw, out, ws)

@@ -33,8 +33,23 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_one_launch_ffn_query():
+    # bf16 decode sizes run gate/up and down as one launch; the deterministic
+    # mode, Int4 weights, prefill sizes and I % 128 != 0 run two
+    one = moe.moe_ffn_one_launch
+    assert one(moe.make_dims(1, 4096, 288, 1536)) == 1
+    assert one(moe.make_dims(64, 4096, 288, 1536)) == 1
+    assert one(moe.make_dims(65, 4096, 288, 1536)) == 0
+    assert one(moe.make_dims(8, 4096, 288, 1536, flags=moe.MOE_FLAG_DETERMINISTIC)) == 0
+    assert one(moe.make_dims(8, 4096, 288, 1536, flags=moe.MOE_FLAG_ACCUMULATE)) == 1
+    assert one(moe.make_dims(8, 4096, 288, 1536, fmt="int4")) == 0
+    assert one(moe.make_dims(8, 256, 288, 64)) == 0
+    assert one(moe.make_dims(8, 384, 288, 256)) == 0     # H not a multiple of 256
+    assert one(moe.make_dims(8, 200, 288, 64)) == -1     # invalid dims
+
+
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 4
+    assert L.moe_abi_version() == 5
     for code in range(6):
         assert moe.moe_status_string(code).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)
@@ -64,9 +79,13 @@ def test_workspace_size(L):
     for ok in (moe.make_dims(8, 12288, 288, 64), moe.make_dims(8, 512, 288, 256, fmt="int4"),
                moe.make_dims((1 << 30) // 9, 256, 288, 64)):
         assert moe.moe_workspace_size(ok) > 0
-    # the deterministic mode keeps (top_k+1)*T*H fp32 rows in the workspace
+    # the deterministic mode keeps (top_k+1)*T*H fp32 rows in the workspace;
+    # it has no use for the one-launch decode FFN's counters (one int per
+    # tile-table entry, at most min(E + 1 + rows / 64, rows) of them, and two
+    # more), which the default mode holds
     det = moe.make_dims(64, 4096, 288, 1536, flags=moe.MOE_FLAG_DETERMINISTIC)
-    assert moe.moe_workspace_size(det) - big >= rows * 4096 * 4
+    counters = (min(288 + 1 + rows // 64, rows) + 2) * 4
+    assert moe.moe_workspace_size(det) - big >= rows * 4096 * 4 - counters - 256
     dense = moe.make_dims(64, 4096, 0, 10240)
     assert moe.moe_dense_workspace_size(dense) >= 64 * 10240 * 4
     assert moe.moe_dense_workspace_size(moe.make_dims(64, 4000, 0, 10240)) == 0

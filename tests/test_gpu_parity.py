@@ -206,6 +206,21 @@ def test_forward_decode(decode, T):
     assert rel_max_err(out, _ref_forward(decode, x)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("T", [1, 8, 17, 64])
+def test_forward_repeated_calls_one_workspace(decode, T):
+    # The fused call keeps counters in its workspace between calls (the
+    # one-launch decode FFN's per-entry counters, the split-K counters, the
+    # routing kernel's CTA counter); they must return to zero after every
+    # call, so that a workspace serves call after call.
+    ws = decode.workspace(T)
+    x0 = decode.inp.x[:T]
+    x2, _, _ = gapped_x(replace(decode.wl, seed=decode.wl.seed + 50), decode.inp.w_router,
+                        decode.inp.b_router, T=T)
+    for rep, x in enumerate((x0, x0[::-1].copy(), x2)):
+        out = decode.forward(x, ws=ws)
+        assert rel_max_err(out, _ref_forward(decode, x)) <= TOL["bf16"], f"call {rep}"
+
+
 def test_forward_ragged_127(decode):
     x = _gapped(decode, 127)
     out = decode.forward(x)
