@@ -903,8 +903,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (gat) go = __shfl_sync(0xffffffffu, go, 0);
         uq.next();
         if (!go || end) break;
-        // the next unit's index, taken now: its round trip overlaps these loads
-        int u_next = lane == 0 ? atomicAdd(a.work, 1) : 0;
         const FfnUnit f = ffn_unit(a, BN, u, wk.nr);
         const TileEntry& te = f.te;
         const bool sh = te.group == a.E;
@@ -951,7 +949,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               phase ^= 1u;
             }
           }
-          u = gat ? __shfl_sync(0xffffffffu, u_next, 0) : u_next;
+          // the next unit, taken once this one's loads are issued (taking it
+          // earlier let the first CTAs to start claim two units each while
+          // the rest of the grid was still being scheduled: measured)
+          u = lane == 0 ? atomicAdd(a.work, 1) : 0;
+          if (gat) u = __shfl_sync(0xffffffffu, u, 0);
           continue;
         }
         const CUtensorMap* mg = sh ? &tm_sgate : &tm_gate;
@@ -1000,7 +1002,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
-        u = gat ? __shfl_sync(0xffffffffu, u_next, 0) : u_next;
+        u = lane == 0 ? atomicAdd(a.work, 1) : 0;
+        if (gat) u = __shfl_sync(0xffffffffu, u, 0);
       }
       // every copy issued has landed before the CTA may exit
       if (lane == 0)
@@ -1160,14 +1163,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before_sync();
           mbar_arrive(&sm.tempty[acc]);
-          __threadfence();
+          // the partials of all four warps are ordered before the count by
+          // the barrier and one GPU-scope fence of the counting thread
           epilogue_bar();
-          if (threadIdx.x == kEpiThread0)
+          if (threadIdx.x == kEpiThread0) {
+            __threadfence();
             sm.split_flags[1] = atomicAdd(&a.counters[tile], 1) == a.ks_g - 1;
+            __threadfence();
+          }
           epilogue_bar();
           wrote = sm.split_flags[1] != 0;
           if (wrote) {
-            __threadfence();
             const float* pt = a.partial + static_cast<size_t>(tile) * a.ks_g * 2 * BN * kBM;
             if (f_out < a.I) {
               for (int c0 = 0; c0 < te.nrows; c0 += 16) {
@@ -1211,10 +1217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&sm.tempty[acc]);
         }
         if (wrote) {
-          // the tile's h rows are visible GPU-wide before the entry counts it
-          __threadfence();
+          // the tile's h rows (all four warps', ordered by the barrier) are
+          // visible GPU-wide before the entry counts it
           epilogue_bar();
           if (threadIdx.x == kEpiThread0) {
+            __threadfence();
             fence_proxy_async_global();
             red_release_gpu_add(&a.ready[f.ei], 1);
           }
