@@ -478,6 +478,70 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
       w[static_cast<size_t>(t) * k + lane] = wv;
     }
   }
+  __syncthreads();
+  if (T <= perm.BN && (!perm.table2 || T <= perm.BN2)) {
+    // Every routed group holds at most T <= BN rows, one tile entry each.  A
+    // pair's row is its rank in (expert, token) order: the pairs of smaller
+    // experts, then this expert's pairs of earlier tokens (a token's ids are
+    // distinct, so pair order is token order within an expert), counted over
+    // the at most kRouteSmallT * k pairs; offsets are binary searches in the
+    // sorted experts and the entries their runs.  No scan, two barriers.
+    __shared__ int s_sorted[kRouteSmallT * kMaxTopK];  // expert of row r < P
+    for (int p = threadIdx.x; p < P; p += kRsThreads) {
+      const int ee = s_e[p];
+      int r = 0;
+      for (int q = 0; q < P; ++q) {
+        const int eq = s_e[q];
+        r += (eq < ee) || (eq == ee && q < p);
+      }
+      s_sorted[r] = ee;
+      perm.gather[r] = p / k;
+      perm.row_of[p] = r;
+      perm.roww[r] = s_w[p];
+    }
+    for (int t = threadIdx.x; t < T; t += kRsThreads) {
+      perm.gather[P + t] = t;
+      perm.roww[P + t] = 1.0f;
+    }
+    __syncthreads();
+    for (int g = threadIdx.x; g <= E + 1; g += kRsThreads) {
+      int lo = 0, hi = P;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_sorted[mid] < g) lo = mid + 1;
+        else hi = mid;
+      }
+      perm.offsets[g] = g <= E ? lo : P + T;  // the shared group E: rows P .. P + T
+    }
+    TileEntry* ent = reinterpret_cast<TileEntry*>(reinterpret_cast<char*>(perm.table) +
+                                                  kTableHeaderBytes);
+    TileEntry* ent2 = perm.table2 ? reinterpret_cast<TileEntry*>(
+                                        reinterpret_cast<char*>(perm.table2) + kTableHeaderBytes)
+                                  : nullptr;
+    for (int r = threadIdx.x; r < P; r += kRsThreads) {
+      const int ee = s_sorted[r];
+      if (r > 0 && s_sorted[r - 1] == ee) continue;  // not the first row of its group
+      int run = 0, end = r + 1;
+      for (int q = 1; q <= r; ++q) run += s_sorted[q] != s_sorted[q - 1];
+      while (end < P && s_sorted[end] == ee) ++end;
+      const TileEntry te{ee, r, end - r, 1};
+      ent[run] = te;
+      if (ent2) ent2[run] = te;
+    }
+    if (threadIdx.x == 0) {
+      int runs = P > 0 ? 1 : 0;
+      for (int q = 1; q < P; ++q) runs += s_sorted[q] != s_sorted[q - 1];
+      const TileEntry te{E, P, T, 1};
+      ent[runs] = te;
+      perm.table[0] = runs + 1;
+      if (ent2) {
+        ent2[runs] = te;
+        perm.table2[0] = runs + 1;
+      }
+      *perm.done = 0;
+    }
+    return;
+  }
   for (int g = threadIdx.x; g <= E; g += kRsThreads) s_off[g] = 0;
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += kRsThreads) atomicAdd(&s_off[s_e[p]], 1);
