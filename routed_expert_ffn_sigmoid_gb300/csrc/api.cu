@@ -539,10 +539,12 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     D.tm_ss[1] = D.tm_ss[0];
     D.table = table;
     D.BN = BN;
-    D.na = 1;
+    // the scatter-add down runs tiles of two 128-row blocks (H % 256 == 0 for Int4)
+    const bool pair = epilogue == kEpiScatterAdd;
+    D.na = pair ? 2 : 1;
     D.K = d.I;
     D.N_out = d.H;
-    D.mblocks = d.H / 128;
+    D.mblocks = d.H / (pair ? 256 : 128);
     D.E = d.E;
     D.total_rows = rows;
     D.out_rows = d.T;

@@ -22,6 +22,10 @@
 //                    written straight into the 128-byte-swizzled operand
 //                    layout the MMA reads
 //   warp 14, lane 0  activation producer: TMA of the token rows (fp16)
+// Two A tiles per operand slot (NA = 2) are gate and up, or, for the down
+// projection with the scatter-add epilogue, two 128-row blocks of the down
+// weights against one token tile (256 output features per tile): each token
+// tile then serves twice the weights and each commit twice the MMAs.
 // The raw ring is as deep as shared memory allows (its stages are what carry
 // the HBM bytes); two to four fp16 weight slots decouple dequantisation from
 // the MMA; the activation tiles have a ring of their own, refilled as soon as
@@ -159,6 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_ss1,
                      const __grid_constant__ CUtensorMap tm_b, const Int4Args a) {
   using Cfg = Int4Cfg<BN, NA>;
+  // down with two row blocks per tile (rows 256 mb .. 256 mb + 255 of one matrix)
+  constexpr bool kPair = NA == 2 && EPI == kEpiScatterAdd;
+  constexpr int kTileRows = kPair ? 2 * kBM : kBM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* slots = base;
@@ -247,14 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << rs;
           armed_par = (armed_par & ~(1u << rs)) | (rph << rs);
           tma_load_3d(code_tile(rs, 0), sh ? &tm_sc0 : &tm_c0, &raw_full[rs], rb * (kRawK / 2),
-                      mb * kBM, ge, pol);
+                      mb * kTileRows, ge, pol);
           tma_load_3d(scale_tile(rs, 0), sh ? &tm_ss0 : &tm_s0, &raw_full[rs], rb * (kRawK / 32),
-                      mb * kBM, ge, pol);
+                      mb * kTileRows, ge, pol);
           if (NA == 2) {
+            // gate/up: the up matrix; paired down: the second row block
+            const int r1 = kPair ? mb * kTileRows + kBM : mb * kBM;
             tma_load_3d(code_tile(rs, 1), sh ? &tm_sc1 : &tm_c1, &raw_full[rs], rb * (kRawK / 2),
-                        mb * kBM, ge, pol);
+                        r1, ge, pol);
             tma_load_3d(scale_tile(rs, 1), sh ? &tm_ss1 : &tm_s1, &raw_full[rs],
-                        rb * (kRawK / 32), mb * kBM, ge, pol);
+                        rb * (kRawK / 32), r1, ge, pol);
           }
           if (++rs == Cfg::kRaw) {
             rs = 0;
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // l + 64, l + 96 -- so the atomics below wait on no global load.
       int tk[4] = {-1, -1, -1, -1};
       float tw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (NA == 1 && EPI == kEpiScatterAdd) {
+      if (EPI == kEpiScatterAdd) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = j * 32 + lane;
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, ab))) break;
       tc_fence_after_sync();
-      const int f = mb * kBM + q * 32 + lane;
+      const int f = mb * kTileRows + q * 32 + lane;
       // column of feature f in the down GEMM's operand order (see dequant8)
       const int f_op = (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1);
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::kAccCols;
@@ -454,29 +463,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x16(tq + c0, v0);
         if (NA == 2) tmem_ld_32x32b_x16(tq + BN + c0, v1);
         tmem_ld_wait();
-        if (NA == 1 && EPI == kEpiScatterAdd) {
+        if (EPI == kEpiScatterAdd) {
           // Lanes 4j .. 4j+3 hold four consecutive features; a 4 x 4 exchange
           // leaves lane 4j+r with those four features of token column
           // 4g + r, added with one 16-byte atomic instead of four scalar ones.
+          // Paired down: the second block's features are 128 further on.
           const int r4 = lane & 3;
-          float* const ob = a.out + (f & ~3);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float x0 = __uint_as_float(v0[4 * g]), x1 = __uint_as_float(v0[4 * g + 1]);
-            float x2 = __uint_as_float(v0[4 * g + 2]), x3 = __uint_as_float(v0[4 * g + 3]);
-            transpose4_lanes(x0, x1, x2, x3, lane);
-            const int cb = c0 + 4 * g;  // a multiple of 4: the same register slot for all lanes
-            const int j = cb >> 5;
-            const int src = (cb + r4) & 31;
-            const int t = __shfl_sync(
-                0xffffffffu, j == 0 ? tk[0] : j == 1 ? tk[1] : j == 2 ? tk[2] : tk[3], src);
-            const float wr = __shfl_sync(
-                0xffffffffu, j == 0 ? tw[0] : j == 1 ? tw[1] : j == 2 ? tw[2] : tw[3], src);
-            const int c = cb + r4;
-            if (c < te.nrows && f < a.N_out) {
-              if (t >= 0)
-                red_add_f32x4(ob + static_cast<size_t>(t) * a.N_out,
-                              make_float4(wr * x0, wr * x1, wr * x2, wr * x3), pol_out);
+          for (int blk = 0; blk < (kPair ? 2 : 1); ++blk) {
+            const int fb = f + blk * kBM;
+            float* const ob = a.out + (fb & ~3);
+            const uint32_t* v = blk ? v1 : v0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float x0 = __uint_as_float(v[4 * g]), x1 = __uint_as_float(v[4 * g + 1]);
+              float x2 = __uint_as_float(v[4 * g + 2]), x3 = __uint_as_float(v[4 * g + 3]);
+              transpose4_lanes(x0, x1, x2, x3, lane);
+              const int cb = c0 + 4 * g;  // a multiple of 4: the same register slot for all lanes
+              const int j = cb >> 5;
+              const int src = (cb + r4) & 31;
+              const int t = __shfl_sync(
+                  0xffffffffu, j == 0 ? tk[0] : j == 1 ? tk[1] : j == 2 ? tk[2] : tk[3], src);
+              const float wr = __shfl_sync(
+                  0xffffffffu, j == 0 ? tw[0] : j == 1 ? tw[1] : j == 2 ? tw[2] : tw[3], src);
+              const int c = cb + r4;
+              if (c < te.nrows && fb < a.N_out) {
+                if (t >= 0)
+                  red_add_f32x4(ob + static_cast<size_t>(t) * a.N_out,
+                                make_float4(wr * x0, wr * x1, wr * x2, wr * x3), pol_out);
+              }
             }
           }
         } else if (f < a.N_out) {
@@ -550,7 +565,9 @@ cudaError_t int4_by_bn(const Int4Launch& L, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s) {
-  if (L.na == 2) return int4_by_bn<2, kEpiStoreRows>(L, s);
+  if (L.na == 2)
+    return L.epilogue == kEpiScatterAdd ? int4_by_bn<2, kEpiScatterAdd>(L, s)
+                                        : int4_by_bn<2, kEpiStoreRows>(L, s);
   if (L.epilogue == kEpiScatterAdd) return int4_by_bn<1, kEpiScatterAdd>(L, s);
   return int4_by_bn<1, kEpiStoreRows>(L, s);
 }

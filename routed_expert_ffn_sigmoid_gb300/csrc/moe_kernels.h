@@ -196,7 +196,9 @@ struct DownLaunch {
 cudaError_t launch_down(const DownLaunch& L, cudaStream_t s);
 
 // Grouped GEMM over grouped-Int4 weights (dequantised in-kernel to fp16).
-// na = 2: gate/up with the clamped SwiGLU, h written as fp16 [rows][N_out];
+// na = 2, store rows: gate/up with the clamped SwiGLU, h written as fp16
+// [rows][N_out]; na = 2, scatter-add: down over tiles of two 128-row blocks
+// (mblocks = N_out / 256; tm_c[1] = tm_c[0], the same for the scales);
 // na = 1: down with the scatter-add or store-rows epilogue.
 struct Int4Launch {
   CUtensorMap tm_c[2], tm_s[2];    // codes / scales of the routed stacks
