@@ -473,7 +473,9 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     D.tm_c[1] = D.tm_c[0];
     D.tm_sc[1] = D.tm_sc[0];
     D.table = down_table;
-    D.na = 1;
+    // the scatter-add down runs tiles of two 128-row blocks (H % 256 == 0 for Int4)
+    const bool pair = epilogue == kEpiScatterAdd;
+    D.na = pair ? 2 : 1;
     D.epilogue = epilogue;
     D.K = d.I;
     D.N_out = d.H;
@@ -489,7 +491,7 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
     D.status = ws.status();
     D.budget_ns = kWaitBudgetNs;
     const int dentries = (d.E + 1) + (rows + kF8DownMaxRows - 1) / kF8DownMaxRows;
-    const int dtiles = dentries * (d.H / 128);
+    const int dtiles = dentries * (d.H / (pair ? 256 : 128));
     D.grid = dtiles < nsm ? dtiles : nsm;
     const cudaError_t e = launch_int4_f8_gemm(D, s);
     record(ev, 4, s);

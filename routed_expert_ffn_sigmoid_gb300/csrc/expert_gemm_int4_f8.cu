@@ -106,10 +106,13 @@ constexpr int kMmaWarp1 = 15;
 constexpr int kIssuers = 2;
 constexpr int kMaxGroups = 128;                    // K / 32 of the down projection (I <= 4096)
 
-template <int NA>
+// NA: weight matrices (A tiles) per operand slot -- gate and up, or for the
+// down projection two 128-row blocks of the down weights against one h tile
+// (kDown with NA = 2) -- or one (down).
+template <int NA, bool kDown>
 struct F8Cfg {
-  static constexpr int kPlanes = NA == 2 ? 2 : 3;             // B rows per token
-  static constexpr int kMaxTok = kBRows / kPlanes;            // 8 or 5
+  static constexpr int kPlanes = kDown ? 3 : 2;               // B rows per token
+  static constexpr int kMaxTok = kBRows / kPlanes;            // 5 or 8
   static constexpr int kGroupCols = 16 * NA;                  // accumulator columns per group
   static constexpr int kEntryCols = kGroupsPerSync * kGroupCols;
   // TMEM: the accumulator ring first, then the operand slots (A, e5m2:
@@ -121,10 +124,10 @@ struct F8Cfg {
   static constexpr int kRawBytes = NA * kCodeTileBytes;
   static constexpr int kRaw = NA == 2 ? 5 : 10;
   static constexpr int kSmemBytes = kRaw * kRawBytes + kBStages * kBStageBytes + 1024 + kBarBytes;
-  static_assert(kSmemBytes <= 227 * 1024 - (NA == 1 ? 4 * kF8DownMaxRows * kMaxGroups * 4 : 0),
+  static_assert(kSmemBytes <= 227 * 1024 - (kDown ? 4 * kF8DownMaxRows * kMaxGroups * 4 : 0),
                 "shared memory");
   static_assert(kABase + kSlots * kACols <= kTmemCols, "TMEM columns");
-  static_assert(kMaxTok == (NA == 2 ? kF8MaxRows : kF8DownMaxRows), "tile entry rows");
+  static_assert(kMaxTok == (kDown ? kF8DownMaxRows : kF8MaxRows), "tile entry rows");
   // one accumulator entry per operand slot: the dequantisers reuse slot n's
   // TMEM columns once acc_full of the entry of slot n - kSlots has completed
   static_assert(kGroupsPerSync == kGroupsPerSlot, "one accumulator entry per slot");
@@ -284,19 +287,21 @@ __device__ __forceinline__ float e4m3_value(uint8_t b) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(b, __NV_E4M3)));
 }
 
-template <int NA, int EPI>
+template <int NA, int EPI, bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
     int4_f8_gemm_kernel(const __grid_constant__ CUtensorMap tm_c0,
                         const __grid_constant__ CUtensorMap tm_c1,
                         const __grid_constant__ CUtensorMap tm_sc0,
                         const __grid_constant__ CUtensorMap tm_sc1,
                         const __grid_constant__ CUtensorMap tm_b, const F8Args a) {
-  using Cfg = F8Cfg<NA>;
+  using Cfg = F8Cfg<NA, kDown>;
   constexpr int P = Cfg::kPlanes;
   constexpr int kTok = Cfg::kMaxTok;
+  // output rows per tile: two 128-row blocks for the paired down
+  constexpr int kTileRows = (kDown && NA == 2) ? 2 * kBM : kBM;
   extern __shared__ uint8_t smem_raw[];
   // down: each epilogue warp's copy of its tile's h scales [token][group]
-  __shared__ float s_hb[NA == 1 ? 4 : 1][NA == 1 ? kTok : 1][NA == 1 ? kMaxGroups : 1];
+  __shared__ float s_hb[kDown ? 4 : 1][kDown ? kTok : 1][kDown ? kMaxGroups : 1];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* raws = base;
   uint8_t* bring = raws + Cfg::kRaw * Cfg::kRawBytes;
@@ -378,10 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << rs;
           armed_par = (armed_par & ~(1u << rs)) | (rph << rs);
           tma_load_3d(code_tile(rs, 0), sh ? &tm_sc0 : &tm_c0, &raw_full[rs], rb * (kRawK / 2),
-                      mb * kBM, ge, pol);
-          if (NA == 2)
+                      mb * kTileRows, ge, pol);
+          if (NA == 2)  // the up matrix, or the down weights' second row block
             tma_load_3d(code_tile(rs, 1), sh ? &tm_sc1 : &tm_c1, &raw_full[rs], rb * (kRawK / 2),
-                        mb * kBM, ge, pol);
+                        kDown ? mb * kTileRows + kBM : mb * kBM, ge, pol);
           if (++rs == Cfg::kRaw) {
             rs = 0;
             rph ^= 1u;
@@ -557,26 +562,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileEntry te = table_entry(a.table, tile / a.mblocks);
       const int mb = tile % a.mblocks;
       const bool sh = te.group == a.E;
-      const int f = mb * kBM + r;  // output feature (N_out % 128 == 0)
+      const int f = mb * kTileRows + r;  // output feature (N_out % 128 == 0)
       const int nt = min(te.nrows, kTok);
       const size_t srow = (static_cast<size_t>(sh ? 0 : te.group) * a.N_out + f) * G;
+      // scales of the second matrix: up's row f, or the second block's row f + 128
+      const size_t srow1 = srow + (kDown ? static_cast<size_t>(kBM) * G : 0);
       const uint4* s0p = reinterpret_cast<const uint4*>((sh ? a.sscale0 : a.scale0) + srow);
-      const uint4* s1p = reinterpret_cast<const uint4*>((sh ? a.sscale1 : a.scale1) + srow);
+      const uint4* s1p = reinterpret_cast<const uint4*>((sh ? a.sscale1 : a.scale1) + srow1);
       // down, scatter-add: lane l < nt holds token l's id and routing weight
       int tk = -1;
       float tw = 0.f;
-      if (NA == 1 && EPI == kEpiScatterAdd && lane < nt && te.row0 + lane < a.total_rows) {
+      if (kDown && EPI == kEpiScatterAdd && lane < nt && te.row0 + lane < a.total_rows) {
         const int t = a.gather[te.row0 + lane];
         tw = a.roww[te.row0 + lane];
         tk = (t >= 0 && t < a.out_rows) ? t : -1;
       }
-      // gate/up: (gate, up) per B column; down: per token
-      float acc0[NA == 2 ? 16 : kTok], acc1[NA == 2 ? 16 : 1];
+      // gate/up: (gate, up) per B column; down: per token (and row block)
+      constexpr int kAcc0 = kDown ? kTok : 16, kAcc1 = NA == 2 ? kAcc0 : 1;
+      float acc0[kAcc0], acc1[kAcc1];
 #pragma unroll
-      for (int c = 0; c < (NA == 2 ? 16 : kTok); ++c) acc0[c] = 0.f;
+      for (int c = 0; c < kAcc0; ++c) acc0[c] = 0.f;
 #pragma unroll
-      for (int c = 0; c < (NA == 2 ? 16 : 1); ++c) acc1[c] = 0.f;
-      if (NA == 1) {
+      for (int c = 0; c < kAcc1; ++c) acc1[c] = 0.f;
+      if (kDown) {
         // the tile's h scales (1 / sigma) for every token and group, loaded
         // once into this warp's shared-memory copy (the warp's previous tile
         // is done with it: all lanes passed its group loop)
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = lane; i < kTok * G; i += 32) {
           const int t = i / G, g = i - t * G;
           const int rr = te.row0 + t;
-          s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g : 0] =
+          s_hb[kDown ? q : 0][kDown ? t : 0][kDown ? g : 0] =
               (t < nt && rr < a.total_rows) ? __ldg(a.binv + static_cast<size_t>(rr) * G + g) : 0.f;
         }
         __syncwarp();
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int gl = 0; gl < kGroupsPerSync; gl += kGroupsPerLoad) {
             const uint32_t tq = tq0 + gl * Cfg::kGroupCols;
             const int gb = gi + gl;  // first group of this load batch within the eight
-            if constexpr (NA == 2) {
+            if constexpr (!kDown) {
               // 2 nt live columns (hi and lo plane of each token)
               if (nt == 1)
                 gateup_batch<2>(tq, s0, s1, gb, acc0, acc1);
@@ -618,25 +626,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 gateup_batch<16>(tq, s0, s1, gb, acc0, acc1);
             } else {
-              // 3 nt live columns (hi, mid and lo plane of each token)
+              // 3 nt live columns (hi, mid and lo plane of each token); with
+              // two row blocks the second block's accumulator is 16 columns on
               auto down_batch = [&](auto wtag) {
                 constexpr int W = decltype(wtag)::value;
                 constexpr int kT = W == 16 ? kTok : W / 3;
-                uint32_t v[kGroupsPerLoad][W];
+                constexpr int kGC = Cfg::kGroupCols;  // 16 or 32
+                uint32_t v[kGroupsPerLoad][NA][W];
 #pragma unroll
-                for (int jj = 0; jj < kGroupsPerLoad; ++jj) tmem_ld_cols<W>(tq + jj * 16, v[jj]);
+                for (int jj = 0; jj < kGroupsPerLoad; ++jj)
+#pragma unroll
+                  for (int m = 0; m < NA; ++m) tmem_ld_cols<W>(tq + jj * kGC + m * 16, v[jj][m]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int jj = 0; jj < kGroupsPerLoad; ++jj) {
                   const float sa = scale_of(s0, gb + jj);
+                  [[maybe_unused]] const float sb = NA == 2 ? scale_of(s1, gb + jj) : 0.f;
 #pragma unroll
                   for (int t = 0; t < kT; ++t) {
-                    const float pv = (__uint_as_float(v[jj][3 * t]) +
-                                      __uint_as_float(v[jj][3 * t + 1])) +
-                                     __uint_as_float(v[jj][3 * t + 2]);
-                    const float hbv =
-                        s_hb[NA == 1 ? q : 0][NA == 1 ? t : 0][NA == 1 ? g8 + gb + jj : 0];
+                    const float hbv = s_hb[kDown ? q : 0][kDown ? t : 0][kDown ? g8 + gb + jj : 0];
+                    const float pv = (__uint_as_float(v[jj][0][3 * t]) +
+                                      __uint_as_float(v[jj][0][3 * t + 1])) +
+                                     __uint_as_float(v[jj][0][3 * t + 2]);
                     acc0[t] = fmaf(sa * hbv, pv, acc0[t]);
+                    if constexpr (NA == 2) {
+                      const float pv1 = (__uint_as_float(v[jj][1][3 * t]) +
+                                         __uint_as_float(v[jj][1][3 * t + 1])) +
+                                        __uint_as_float(v[jj][1][3 * t + 2]);
+                      acc1[t] = fmaf(sb * hbv, pv1, acc1[t]);
+                    }
                   }
                 }
               };
@@ -659,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s1 = s1n;
       }
       if (!ok) break;
-      if (NA == 2) {
+      if (!kDown) {
         // SwiGLU, then h as three e4m3 planes under a power-of-two scale per
         // (token, group of 32 features): the warp's 32 lanes are one group
         const int g32 = f >> 5;
@@ -694,20 +712,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (EPI == kEpiScatterAdd) {
         // lanes 4j .. 4j+3 hold four consecutive features: a 4 x 4 exchange
         // gives lane 4j+r those features of token tg + r, one 16-byte atomic
+        // (two row blocks: the second block's features are 128 further on)
         const int r4 = lane & 3;
-        float* const ob = a.out + (f & ~3);
 #pragma unroll
-        for (int tg = 0; tg < kTok; tg += 4) {
-          float x[4];
+        for (int m = 0; m < NA; ++m) {
+          float* const ob = a.out + ((f + m * kBM) & ~3);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) x[i] = tg + i < kTok ? acc0[(tg + i) % kTok] : 0.f;
-          transpose4_lanes(x[0], x[1], x[2], x[3], lane);
-          const int t = tg + r4;
-          const int tok = __shfl_sync(0xffffffffu, tk, t & 31);
-          const float wr = __shfl_sync(0xffffffffu, tw, t & 31);
-          if (t < nt && tok >= 0)
-            atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(tok) * a.N_out),
-                      make_float4(wr * x[0], wr * x[1], wr * x[2], wr * x[3]));
+          for (int tg = 0; tg < kTok; tg += 4) {
+            float x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int ti = (tg + i) % kTok;
+              x[i] = tg + i < kTok ? (m == 0 ? acc0[ti] : acc1[NA == 2 ? ti : 0]) : 0.f;
+            }
+            transpose4_lanes(x[0], x[1], x[2], x[3], lane);
+            const int t = tg + r4;
+            const int tok = __shfl_sync(0xffffffffu, tk, t & 31);
+            const float wr = __shfl_sync(0xffffffffu, tw, t & 31);
+            if (t < nt && tok >= 0)
+              atomicAdd(reinterpret_cast<float4*>(ob + static_cast<size_t>(tok) * a.N_out),
+                        make_float4(wr * x[0], wr * x[1], wr * x[2], wr * x[3]));
+          }
         }
       } else {
 #pragma unroll
@@ -725,14 +750,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NA, int EPI>
+template <int NA, int EPI, bool kDown>
 cudaError_t f8_dispatch(const Int4F8Launch& L, cudaStream_t s) {
-  using Cfg = F8Cfg<NA>;
-  auto kern = int4_f8_gemm_kernel<NA, EPI>;
+  using Cfg = F8Cfg<NA, kDown>;
+  auto kern = int4_f8_gemm_kernel<NA, EPI, kDown>;
+  constexpr int kTileRows = (kDown && NA == 2) ? 2 * kBM : kBM;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  F8Args a{L.table, L.K, L.N_out, L.N_out / kBM, L.E, L.total_rows, L.out_rows,
+  F8Args a{L.table, L.K, L.N_out, L.N_out / kTileRows, L.E, L.total_rows, L.out_rows,
            static_cast<const uint16_t*>(L.scale[0]), static_cast<const uint16_t*>(L.scale[1]),
            static_cast<const uint16_t*>(L.sscale[0]), static_cast<const uint16_t*>(L.sscale[1]),
            L.binv, L.h8, L.hinv, L.gather, L.roww, L.out, L.status, L.budget_ns};
@@ -754,10 +780,17 @@ cudaError_t f8_dispatch(const Int4F8Launch& L, cudaStream_t s) {
 cudaError_t launch_int4_f8_gemm(const Int4F8Launch& L, cudaStream_t s) {
   if (L.K % kRawK != 0 || L.N_out % kBM != 0) return cudaErrorInvalidValue;
   // down keeps the tile's h scales (K / 32 per token) in static shared memory
-  if (L.na == 1 && L.K / 32 > kMaxGroups) return cudaErrorInvalidValue;
-  if (L.na == 2) return f8_dispatch<2, kEpiStoreRows>(L, s);
-  if (L.epilogue == kEpiScatterAdd) return f8_dispatch<1, kEpiScatterAdd>(L, s);
-  return f8_dispatch<1, kEpiStoreRows>(L, s);
+  // down (epilogue scatter-add or store rows; na = 2: two row blocks per
+  // tile, scatter-add only) keeps the tile's h scales in static shared memory
+  const bool down = L.epilogue != kEpiStoreRows || L.na == 1;
+  if (down && L.K / 32 > kMaxGroups) return cudaErrorInvalidValue;
+  if (L.na == 2 && L.epilogue == kEpiScatterAdd) {
+    if (L.N_out % (2 * kBM) != 0) return cudaErrorInvalidValue;
+    return f8_dispatch<2, kEpiScatterAdd, true>(L, s);
+  }
+  if (L.na == 2) return f8_dispatch<2, kEpiStoreRows, false>(L, s);
+  if (L.epilogue == kEpiScatterAdd) return f8_dispatch<1, kEpiScatterAdd, true>(L, s);
+  return f8_dispatch<1, kEpiStoreRows, true>(L, s);
 }
 
 }  // namespace moe

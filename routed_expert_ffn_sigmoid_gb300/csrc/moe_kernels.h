@@ -226,6 +226,9 @@ cudaError_t launch_int4_gemm(const Int4Launch& L, cudaStream_t s);
 //           hinv [rows][N_out / 32] = 1 / sigma per group of 32 features.
 //   na = 1: down with the scatter-add or store-rows epilogue.  B: those h
 //           planes, binv = hinv; tile entries of at most kF8DownMaxRows rows.
+//   na = 2 with the scatter-add epilogue: the same down over tiles of two
+//           128-row blocks (N_out % 256 == 0; tm_c[1] = tm_c[0], scale[1] =
+//           scale[0], the same for the shared expert).
 constexpr int kF8MaxRows = 8;
 constexpr int kF8DownMaxRows = 5;
 struct Int4F8Launch {
