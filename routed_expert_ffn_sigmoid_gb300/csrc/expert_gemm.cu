@@ -1164,13 +1164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before_sync();
           mbar_arrive(&sm.tempty[acc]);
           // the partials of all four warps are ordered before the count by
-          // the barrier and one GPU-scope fence of the counting thread
+          // the barrier and the counting thread's release; its acquire
+          // orders the finisher's partial loads after the other parts' counts
           epilogue_bar();
-          if (threadIdx.x == kEpiThread0) {
-            __threadfence();
-            sm.split_flags[1] = atomicAdd(&a.counters[tile], 1) == a.ks_g - 1;
-            __threadfence();
-          }
+          if (threadIdx.x == kEpiThread0)
+            sm.split_flags[1] = atom_acq_rel_gpu_add(&a.counters[tile], 1) == a.ks_g - 1;
           epilogue_bar();
           wrote = sm.split_flags[1] != 0;
           if (wrote) {
@@ -1221,7 +1219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // visible GPU-wide before the entry counts it
           epilogue_bar();
           if (threadIdx.x == kEpiThread0) {
-            __threadfence();
             fence_proxy_async_global();
             red_release_gpu_add(&a.ready[f.ei], 1);
           }

@@ -119,6 +119,16 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
+// One acquire-release add at GPU scope: the thread's earlier writes (and,
+// through a barrier before it, its CTA's) are ordered before it, its later
+// reads after it; returns the old value.
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

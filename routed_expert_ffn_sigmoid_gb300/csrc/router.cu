@@ -446,13 +446,15 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
       z[static_cast<size_t>(t) * E + e2] =
           ((red[l2][0][t] + red[l2][1][t]) + (red[l2][2][t] + red[l2][3][t])) + b[e2];
   }
-  // the last CTA to finish selects and permutes
-  __threadfence();
+  // The last CTA to finish selects and permutes.  The CTA's logits are
+  // ordered before its count by the barrier and the counting thread's
+  // release; the last CTA's acquire orders its reads of every CTA's logits
+  // after their counts.
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(perm.done, 1) == static_cast<int>(gridDim.x) - 1;
+  if (threadIdx.x == 0)
+    s_last = atom_acq_rel_gpu_add(perm.done, 1) == static_cast<int>(gridDim.x) - 1;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   __shared__ int s_e[kRouteSmallT * kMaxTopK];
   __shared__ float s_w[kRouteSmallT * kMaxTopK];
