@@ -456,6 +456,7 @@ def run_ours(args, wl, rank, world, local):
     # the dominant kernel: gate/up, or with one launch gate/up + down together
     # (the timed call's gate/up stage then brackets both projections)
     one_launch = moe.moe_ffn_one_launch(dims) == 1
+    int4_gemv = moe.moe_ffn_int4_gemv(dims) == 1
     gu_ms = statistics.mean(stage_ms[2])
     gu_bytes = statistics.mean(
         gateup_bytes(wl, distinct[s % N_BATCHES])
@@ -481,6 +482,8 @@ def run_ours(args, wl, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("bf16 operands, fp32 accumulate" if wl.fmt == "bf16" else
+                      "int4 codes x 16-bit activations (two byte planes) in int8 dot products, "
+                      "exact int32 group sums, scale per group in fp32" if int4_gemv else
                       "int4 weights as e5m2 (n - 8) x e4m3 activation planes, scale per group "
                       "after the MMA, fp32 accumulate" if wl.T <= 64 else
                       "int4 weights dequantised to fp16, fp32 accumulate"),
@@ -488,6 +491,7 @@ def run_ours(args, wl, rank, world, local):
             "config": config_of(wl, world, args, one_launch),
             "roofline": {"bound": "hbm",
                          "kernel": ("decode_ffn (tcgen05 gate/up + down, one launch)" if one_launch
+                                    else "int4_gemv_gateup (CUDA-core dp4a gate/up)" if int4_gemv
                                     else "gateup_swiglu (tcgen05 grouped gate/up)"),
                          "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,

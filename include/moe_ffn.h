@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 5
+#define MOE_FFN_ABI_VERSION 6
 
 /* A cudaStream_t, spelled without the CUDA headers. */
 typedef struct CUstream_st* moe_stream_t;
@@ -187,7 +187,14 @@ moe_status moe_combine(const moe_dims* d, const float* y_perm, const int32_t* ro
  * routing weight and adds into out (fp32 [T][H]), with the shared expert run
  * as one more group of weight 1.  By default out is overwritten and the fp32
  * additions into it are atomic, so the last bits may differ run to run.
- * Int4 weights up to 64 tokens run on 8-bit tensor-core operands: the codes
+ * Int4 weights up to 32 tokens with H a multiple of 1024 up to 4096 and I a
+ * multiple of 512 up to 2048 run on CUDA cores: 8-bit integer dot products of
+ * the codes against x and h quantised to 16 bits under a power-of-two scale
+ * per row and group of 32 (x exactly for entries within 2^-7 of their group's
+ * largest |x|, within 2^-15 of it below; h within 2^-14 of its group's
+ * largest |h|), exact integer group sums, each group's scale applied in fp32.
+ * Other Int4 shapes up to 64 tokens (and these from 33 tokens) run on 8-bit
+ * tensor-core operands: the codes
  * as e5m2 (n - 8, exact), x and h as e4m3 planes under power-of-two scales
  * (x exactly for entries at least 2^-9 of their row's largest |x|, within
  * 2^-17 of it below; h within 2^-12 relative near each 32-feature group's
@@ -325,6 +332,15 @@ moe_status moe_tp_slice_weights(const moe_dims* d, int32_t n_experts, int32_t pa
  * empty.  Host-only; launches nothing.
  */
 int moe_ffn_one_launch(const moe_dims* d);
+
+/*
+ * How moe_ffn_forward runs Int4 expert weights for these dims: 1 when gate/up
+ * and down run on CUDA cores with 8-bit integer dot products (Int4 weights,
+ * up to 32 tokens, H a multiple of 1024 up to 4096, I a multiple of 512 up to
+ * 2048), 0 otherwise (tensor-core kernels), -1 for invalid dims.  For
+ * profilers and benchmarks.  Host-only; launches nothing.
+ */
+int moe_ffn_int4_gemv(const moe_dims* d);
 
 /*
  * Synchronises `stream`, returns the device status word that kernels using

@@ -37,7 +37,8 @@ EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_size", "moe_ro
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
            "moe_ffn_forward_timed", "moe_workspace_status", "moe_debug_wait_timeout",
            "moe_router_topk_static_scratch", "moe_dense_workspace_size", "moe_dense_ffn",
-           "moe_workspace_routing", "moe_tp_slice_weights", "moe_ffn_one_launch")
+           "moe_workspace_routing", "moe_tp_slice_weights", "moe_ffn_one_launch",
+           "moe_ffn_int4_gemv")
 
 # T * E limit of moe_router_topk_static_scratch (floats of its fixed scratch)
 MOE_STATIC_ROUTER_LOGITS = 1 << 18
@@ -109,6 +110,7 @@ def lib() -> ctypes.CDLL:
                 "moe_workspace_routing": ([pd, vp, sz, ctypes.POINTER(MoeRoutingView)], i32),
                 "moe_tp_slice_weights": ([pd, i32, i32, i32, pw, pw, vp], i32),
                 "moe_ffn_one_launch": ([pd], i32),
+                "moe_ffn_int4_gemv": ([pd], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -243,6 +245,12 @@ def moe_ffn_one_launch(dims) -> int:
     """1 when moe_ffn_forward runs gate/up and down as one launch for these
     dims, 0 for two launches, -1 for invalid dims (include/moe_ffn.h)."""
     return int(lib().moe_ffn_one_launch(ctypes.byref(dims)))
+
+
+def moe_ffn_int4_gemv(dims) -> int:
+    """1 when moe_ffn_forward runs Int4 gate/up and down on CUDA cores for
+    these dims, 0 otherwise, -1 for invalid dims (include/moe_ffn.h)."""
+    return int(lib().moe_ffn_int4_gemv(ctypes.byref(dims)))
 
 
 def moe_workspace_routing(dims, ws) -> MoeRoutingView:

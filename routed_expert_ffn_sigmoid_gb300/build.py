@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_ffn.so")
 SOURCES = ["api.cu", "router.cu", "permute.cu", "combine.cu", "expert_gemm.cu",
-           "expert_gemm_int4.cu", "expert_gemm_int4_f8.cu", "expert_gemm_tm.cu"]
+           "expert_gemm_int4.cu", "expert_gemm_int4_f8.cu", "expert_gemm_tm.cu",
+           "expert_gemv_int4.cu"]
 HEADERS = ["ptx.cuh", "moe_kernels.h", "route_common.cuh", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

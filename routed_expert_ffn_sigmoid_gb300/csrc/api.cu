@@ -47,15 +47,29 @@ int pick_bn(int T) {
   return 128;
 }
 
-// Int4 weights up to 64 tokens: gate/up and down both on 8-bit operands
-// (gate/up entries of at most kF8MaxRows rows, down entries of at most
-// kF8DownMaxRows rows in a table of their own).
+// Int4 weights up to kInt4GemvMaxTokens tokens, in the shapes the CUDA-core
+// kernels take: gate/up and down as GEMVs with 8-bit integer dot products
+// (entries of at most kGemvMaxRows rows).  Measured against the 8-bit
+// tcgen05 kernels (decode shapes, full layer): 1 token 44.2 vs 64.8 us, 8
+// tokens 192.2 vs 206.1, 32 tokens 475.2 vs 516.5, 64 tokens 751.6 vs 730.5.
+constexpr int kInt4GemvMaxTokens = 32;
+
+bool int4_gemv(const moe_dims& d) {
+  return d.fmt == MOE_W_INT4_G32 && d.T <= kInt4GemvMaxTokens && d.top_k > 0 &&
+         int4_gemv_shape_ok(d.H, d.I);
+}
+
+// Other Int4 shapes up to 64 tokens: gate/up and down both on 8-bit
+// tensor-core operands (gate/up entries of at most kF8MaxRows rows, down
+// entries of at most kF8DownMaxRows rows in a table of their own).
 bool int4_f8(const moe_dims& d) {
-  return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0 && d.I <= 4096;
+  return d.fmt == MOE_W_INT4_G32 && d.T <= 64 && d.top_k > 0 && d.I <= 4096 && !int4_gemv(d);
 }
 
 // Rows per tile-table entry of the fused layer.
-int table_bn(const moe_dims& d) { return int4_f8(d) ? kF8MaxRows : pick_bn(d.T); }
+int table_bn(const moe_dims& d) {
+  return int4_gemv(d) ? kGemvMaxRows : int4_f8(d) ? kF8MaxRows : pick_bn(d.T);
+}
 
 size_t table_bytes(const moe_dims& d) {
   // every group contributes at most ceil(cnt / BN) entries with BN >= 5 (the
@@ -150,7 +164,9 @@ Layout layout_of(const moe_dims& d) {
   L.xinv = take(int4_f8(d) ? rows * 4 : 0);
   L.h0 = take(rows * I * (int4_f8(d) ? 3 : 2));  // 8-bit path: three e4m3 planes of h
   L.h1 = take(d.fmt == MOE_W_BF16 ? rows * I * 2 : 0);
-  L.hinv = take(int4_f8(d) ? rows * (I / 32) * 4 : 0);
+  // 8-bit path: 1 / sigma per row and group of h; CUDA-core path: sigma and
+  // 8 sum q per row and group of h
+  L.hinv = take(int4_f8(d) ? rows * (I / 32) * 4 : int4_gemv(d) ? rows * (I / 32) * 8 : 0);
   L.y_perm = take((d.flags & MOE_FLAG_DETERMINISTIC) ? rows * H * 4 : 0);
   const int tiles = gateup_tiles_bound(d);
   L.partial_units = tiles < kSplitTileLimit ? static_cast<size_t>(tiles) * kMaxSplit : 0;
@@ -430,6 +446,50 @@ moe_status run_experts(const moe_dims& d, const void* x_perm, const int32_t* tab
                        const void* x_shared_first = nullptr) {
   const int rows = rows_of(d);
   const int nsm = sm_count();
+  if (d.fmt == MOE_W_INT4_G32 && xrows && int4_gemv(d)) {
+    // CUDA-core GEMVs: gate/up quantises the rows x[xrows[r]] itself and
+    // writes h as 16-bit planes, down reads them through the same table
+    Int4GemvLaunch G{};
+    G.table = table;
+    G.E = d.E;
+    G.total_rows = rows;
+    G.out_rows = d.T;
+    G.x = static_cast<const uint16_t*>(x_perm);
+    G.xrows = xrows;
+    G.hq = ws.at<uint8_t>(ws.L.h0);
+    G.hs = ws.at<float>(ws.L.hinv);
+    G.hc = reinterpret_cast<int32_t*>(G.hs + static_cast<size_t>(rows) * (d.I / 32));
+    Int4GemvLaunch D = G;
+    G.K = d.H;
+    G.N_out = d.I;
+    G.codes[0] = ex->gate;
+    G.codes[1] = ex->up;
+    G.scale[0] = ex->gate_scale;
+    G.scale[1] = ex->up_scale;
+    G.scodes[0] = sh->gate;
+    G.scodes[1] = sh->up;
+    G.sscale[0] = sh->gate_scale;
+    G.sscale[1] = sh->up_scale;
+    const long entries = std::min<long>((d.E + 1) + (rows + kGemvMaxRows - 1) / kGemvMaxRows, rows);
+    G.grid = static_cast<int>(std::min<long>(entries * (d.I / 32), 2L * nsm));
+    record(ev, 2, s);
+    if (launch_int4_gemv_gateup(G, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(ev, 3, s);
+    D.epilogue = epilogue;
+    D.K = d.I;
+    D.N_out = d.H;
+    D.codes[0] = D.codes[1] = ex->down;
+    D.scale[0] = D.scale[1] = ex->down_scale;
+    D.scodes[0] = D.scodes[1] = sh->down;
+    D.sscale[0] = D.sscale[1] = sh->down_scale;
+    D.gather = gather;
+    D.roww = roww;
+    D.out = out;
+    D.grid = static_cast<int>(std::min<long>(entries * (d.H / 128), 2L * nsm));
+    const cudaError_t e = launch_int4_gemv_down(D, s);
+    record(ev, 4, s);
+    return from_cuda(e);
+  }
   if (d.fmt == MOE_W_INT4_G32 && xinv && down_table) {
     // 8-bit operands: x_perm holds the e4m3 planes of x; gate/up writes h as
     // three planes, down reads them through its own table
@@ -775,13 +835,15 @@ moe_status forward_impl(const moe_dims* d, const void* x, const void* w_router,
   // kTmGatherMinTokens tokens in the token-major kernels by cp.async from a
   // gather warp (measured: -3.1 % per step at 4096 tokens, -0.6 % at 512,
   // +0.8 % at 128).  Int4 needs the fp16 copy in its operand order, or up
-  // to 64 tokens the two e4m3 planes of the 8-bit gate/up kernel.
+  // to 64 tokens the two e4m3 planes of the 8-bit gate/up kernel, except in
+  // the CUDA-core kernels, which quantise the rows of x themselves.
   const bool int4 = d->fmt == MOE_W_INT4_G32;
   const bool f8 = int4_f8(*d);
+  const bool gemv = int4_gemv(*d);
   float* xinv = f8 ? w.at<float>(L.xinv) : nullptr;
   const bool tm = token_major(*d);
   const bool rows_from_x =
-      !int4 && (d->T <= kGatherFromXTokens || (tm && d->T >= kTmGatherMinTokens));
+      gemv || (!int4 && (d->T <= kGatherFromXTokens || (tm && d->T >= kTmGatherMinTokens)));
   // who clears out: the gather kernel when it runs, else the token-major
   // gate/up kernel's idle epilogue warps, else the router's kernels
   float* zero_gather = rows_from_x ? nullptr : zero_out;
@@ -1015,6 +1077,11 @@ moe_status moe_dense_ffn(const moe_dims* d, const void* x, const moe_weights* we
 int moe_ffn_one_launch(const moe_dims* d) {
   if (check_dims(d) != MOE_OK) return -1;
   return one_launch_ffn(*d) ? 1 : 0;
+}
+
+int moe_ffn_int4_gemv(const moe_dims* d) {
+  if (check_dims(d) != MOE_OK) return -1;
+  return int4_gemv(*d) ? 1 : 0;
 }
 
 moe_status moe_workspace_routing(const moe_dims* d, const void* ws, size_t ws_bytes,

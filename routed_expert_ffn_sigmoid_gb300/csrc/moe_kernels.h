@@ -251,6 +251,38 @@ struct Int4F8Launch {
 };
 cudaError_t launch_int4_f8_gemm(const Int4F8Launch& L, cudaStream_t s);
 
+// Int4 grouped GEMVs on CUDA cores (decode sizes): 8-bit integer dot products
+// of the codes against the activation rows quantised to 16 bits (a signed
+// high and an unsigned low byte) under a power-of-two scale per row and group
+// of 32; tile entries of at most kGemvMaxRows rows.  Shapes: K = H a multiple
+// of 1024 up to 4096, I a multiple of 512 up to 2048 (int4_gemv_shape_ok).
+//   gate/up: token rows x[xrows[r]] (bf16 [.][K]), N_out = I; writes h as
+//            planes hq [rows][4][I / 32] x 16 bytes, the scales hs [rows][I / 32]
+//            and 8 sum q hc [rows][I / 32].
+//   down:    K = I, N_out = H; reads those planes; scatter-add (out [out_rows][H]
+//            += roww[r] y, token gather[r]) or store rows (out = y_perm [rows][H]).
+// codes[1] / scale[1] / scodes[1] / sscale[1] are unused by down.
+constexpr int kGemvMaxRows = 8;
+struct Int4GemvLaunch {
+  const int32_t* table;
+  int epilogue, K, N_out, E, total_rows, out_rows, grid;
+  const uint16_t* x;
+  const int32_t* xrows;
+  const void* codes[2];    // routed stacks [E][N_out][K / 2]
+  const void* scale[2];    // bf16 [E][N_out][K / 32]
+  const void* scodes[2];   // the shared expert's
+  const void* sscale[2];
+  uint8_t* hq;
+  float* hs;
+  int32_t* hc;
+  const int32_t* gather;
+  const float* roww;
+  float* out;
+};
+bool int4_gemv_shape_ok(int H, int I);
+cudaError_t launch_int4_gemv_gateup(const Int4GemvLaunch& L, cudaStream_t s);
+cudaError_t launch_int4_gemv_down(const Int4GemvLaunch& L, cudaStream_t s);
+
 // Token-major grouped GEMM (bf16, token tiles of 128 rows): gate/up with the
 // SwiGLU epilogue (h hi/lo planes) or down with the scatter-add / store-rows
 // epilogue.  tm_a: token planes (x_perm; or h hi, h lo), tm_b / tm_sb: weight

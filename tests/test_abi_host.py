@@ -23,7 +23,7 @@ def L():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(L):
@@ -48,8 +48,25 @@ def test_one_launch_ffn_query():
     assert one(moe.make_dims(8, 200, 288, 64)) == -1     # invalid dims
 
 
+def test_int4_gemv_query():
+    # Int4 decode shapes up to 32 tokens run on CUDA cores; 33 tokens and
+    # above, bf16, and shapes outside H % 1024 / I % 512 (or H > 4096,
+    # I > 2048) run the tensor-core kernels
+    q = moe.moe_ffn_int4_gemv
+    assert q(moe.make_dims(1, 4096, 288, 1536, fmt="int4")) == 1
+    assert q(moe.make_dims(32, 4096, 288, 1536, fmt="int4")) == 1
+    assert q(moe.make_dims(33, 4096, 288, 1536, fmt="int4")) == 0
+    assert q(moe.make_dims(8, 4096, 288, 1536)) == 0
+    assert q(moe.make_dims(8, 4096, 288, 4096, fmt="int4")) == 0
+    assert q(moe.make_dims(8, 3072, 288, 512, fmt="int4")) == 1
+    assert q(moe.make_dims(8, 2560, 288, 512, fmt="int4")) == 0
+    assert q(moe.make_dims(8, 8192, 288, 512, fmt="int4")) == 0
+    assert q(moe.make_dims(8, 4096, 288, 768, fmt="int4")) == 0
+    assert q(moe.make_dims(8, 200, 288, 64, fmt="int4")) == -1
+
+
 def test_abi_version_and_status_strings(L):
-    assert L.moe_abi_version() == 5
+    assert L.moe_abi_version() == 6
     for code in range(6):
         assert moe.moe_status_string(code).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)
