@@ -509,7 +509,7 @@ def run_ours(args, wl, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 4},
             # T <= 128: logits, one-CTA routing, gather, gate/up, down; larger T:
-            "gpu_launches": (layer_launches(wl.T, args.deterministic, wl.fmt)
+            "gpu_launches": (layer_launches(wl.T, args.deterministic, wl.fmt, int4_gemv)
                              - (1 if one_launch else 0)) * args.steps,
             "clocks": clk.summary(),
         }
@@ -635,7 +635,8 @@ def time_config(moe, dev, wl, layer, host_x, w_router_np, b_router_np, experts_n
             "ms_p10": float(np.percentile(step_ms, 10)), "ms_p90": float(np.percentile(step_ms, 90)),
             "value": wl.T / (ms / 1e3), "unit": "tokens/s", "GBps": gbs, "TFLOPps": tflops,
             "distinct_experts_mean": mean_distinct, "roofline": roof,
-            "gpu_launches": (layer_launches(wl.T, False, wl.fmt)
+            "gpu_launches": (layer_launches(wl.T, False, wl.fmt,
+                                            moe.moe_ffn_int4_gemv(dims) == 1)
                              - (1 if moe.moe_ffn_one_launch(dims) == 1 else 0)) * steps,
             "clocks": clk.summary(), "cpu_baseline": cpu}
 
@@ -679,16 +680,17 @@ def per_config_block(args, dev, resident=None):
     return entries
 
 
-def layer_launches(T, deterministic, fmt="bf16"):
+def layer_launches(T, deterministic, fmt="bf16", int4_gemv=False):
     """Kernels one moe_ffn_forward launches.  T <= 128: router partial logits,
     slice sum + top-k, the one-CTA permutation (for T <= 16 run by the top-k
     kernel's last CTA instead), gate/up, down.
     Larger T: logits (partial sums below 256 tokens, tensor cores from 256),
     top-k, count, scan, scatter, gate/up, down.  The bf16 gate/up GEMM gathers
     the token rows from x itself up to 8 tokens and from 512 tokens (its
-    token-major form); in between, and always for Int4, one more kernel writes
-    x_perm.  Deterministic mode adds the fixed-order combination."""
-    gathers_itself = fmt == "bf16" and (T <= 8 or T >= 512)
+    token-major form), and so does the CUDA-core Int4 gate/up (int4_gemv); in
+    between, and otherwise for Int4, one more kernel writes x_perm.
+    Deterministic mode adds the fixed-order combination."""
+    gathers_itself = int4_gemv or (fmt == "bf16" and (T <= 8 or T >= 512))
     base = 4 if T <= 16 else (5 if T <= 128 else 7)
     return base + (0 if gathers_itself else 1) + (1 if deterministic else 0)
 
