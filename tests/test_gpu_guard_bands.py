@@ -5,9 +5,10 @@ workspace (so that the counters the calls keep in it are reused) the
 margins must be unchanged, the status word clear and the output equal to
 the oracle's.  The sizes cover every path of the fused call: the one-launch
 decode FFN (bf16, 1..64 tokens), the token-major kernels with the token rows
-from x_perm (65..511) and gathered from x (512 and more), the 8-bit Int4
-kernels (up to 64 tokens), the fp16-operand Int4 kernels with the paired down
-projection, and the deterministic and accumulate modes."""
+from x_perm (65..511) and gathered from x (512 and more), the CUDA-core Int4
+GEMVs (up to 32 tokens), the 8-bit Int4 kernels (33..64 tokens), the
+fp16-operand Int4 kernels with the paired down projection, and the
+deterministic and accumulate modes."""
 from dataclasses import replace
 
 import numpy as np
