@@ -186,8 +186,8 @@ def test_skewed_prefill_scatter_add_matches_deterministic(skewed4):
 @pytest.mark.parametrize("T", [16, 17, 33])
 def test_forward_decode_int4_token_counts(decode4, T):
     # Around the one-CTA permutation's boundaries (fused into the router up
-    # to 16 tokens); up to 64 tokens gate/up runs on 8-bit operands with tile
-    # entries of at most 8 rows and down on its own table.
+    # to 16 tokens) and the paths' (up to 32 tokens the CUDA-core GEMVs, 33
+    # to 64 the 8-bit kernels); tile entries of at most 8 rows.
     x = decode4.inp.x[:T]
     out = decode4.forward(x)
     assert rel_max_err(out, _ref(decode4, x)) <= TOL["int4"]
@@ -214,11 +214,12 @@ def test_forward_int4_all_tokens_one_expert_set_decode(decode4):
     assert rel_max_err(out[sample], ref) <= TOL["int4"]
 
 
-def test_forward_int4_row_scales(decode4):
-    # The 8-bit path scales each token row by a power of two from its
-    # largest |x|: a row of zeros, rows of tiny and of large values, and a
-    # row with one large value among small ones, against the oracle.
-    T = 8
+@pytest.mark.parametrize("T", [8, 40])
+def test_forward_int4_row_scales(decode4, T):
+    # Power-of-two activation scales from the largest |x| of each group of 32
+    # of a row (CUDA-core GEMVs, 8 tokens) or of each row (8-bit kernels, 40
+    # tokens): a row of zeros, rows of tiny and of large values, and a row
+    # with one large value among small ones, against the oracle.
     x = decode4.inp.x[:T].copy()
     xf = synthetic.bf16_bits_to_f32(x)
     xf[0] = 0.0
