@@ -84,14 +84,12 @@ def test_workspace_size(L):
     assert big >= rows * 4096 * 2 + 2 * rows * 1536 * 2
     d4 = moe.make_dims(64, 4096, 288, 1536, fmt="int4")
     assert moe.moe_workspace_size(d4) < big  # one fp16 plane of h instead of two
-    # Int4 on CUDA cores (32 tokens): the x_perm region (which holds each
-    # token's 16-bit planes, T H 2 bytes, and its scales and 8 sum q, T H / 4
-    # bytes), h as 16-bit planes (rows I 2 bytes) and two words per row and
-    # group of 32 features of h
+    # Int4 on CUDA cores (32 tokens): h as 16-bit planes (rows I 2 bytes)
+    # and two words (sigma, 8 sum q) per row and group of 32 features of h,
+    # beside the x_perm region every layout reserves
     g4 = moe.make_dims(32, 4096, 288, 1536, fmt="int4")
     assert moe.moe_ffn_int4_gemv(g4) == 1
     r4 = 9 * 32
-    assert r4 * 4096 * 2 >= 32 * 4096 * 2 + 32 * 4096 // 4
     assert moe.moe_workspace_size(g4) >= r4 * 4096 * 2 + r4 * 1536 * 2 + r4 * (1536 // 32) * 8
     for bad in (moe.make_dims(8, 200, 288, 64), moe.make_dims(8, 256, 288, 96),
                 moe.make_dims(8, 256, 600, 64), moe.make_dims(8, 256, 288, 64, top_k=17),
