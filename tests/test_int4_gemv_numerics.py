@@ -1,0 +1,99 @@
+"""Precision of the Int4 decode GEMVs on CUDA cores, modelled on the CPU at
+the decode shape (H = 4096, I = 1536, Int4 weights of the synthetic decode
+workload) and compared with the oracle's expert FFN.
+
+The model takes the transforms of that path and nothing else: x and h
+quantised to 16-bit integers under a power-of-two scale per token and group
+of 32 (the group's largest |a| in [2^14, 2^15) sigma, q clamped to +-32767),
+the integer group sums sum (n - 8) q (exact, as the dp4a sums are), each
+converted to fp32 and scaled by s_g sigma_g, and the fp32 sums over groups
+and the SwiGLU in fp32.  It pins what the design rests on: the 16-bit
+activations keep the expert output far inside the Int4 tolerance (5e-3 of
+RMS), tighter than fp16 h would.  Measured with this model: max err / RMS
+2.3e-4, nearly all of it h's quantisation (2.6e-4 alone; x's 2.7e-5): the
+clamped SwiGLU reaches |h| ~ 100 on this workload, and a group's small
+values share the quantum of its largest one (2^-15 of it).  The offset-binary decode, value = (nibble
+- 8) * scale, is the grouped fmt=4 format of "feat(glm53): add
+device-resident HIP backend for MI350P", "Key changes".
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from moe_inputs import rel_max_err
+
+T = 8
+G = synthetic.INT4_GROUP
+
+
+def _codes(codes):
+    n = np.empty((codes.shape[0], 2 * codes.shape[1]), np.int64)
+    n[:, 0::2] = codes & 15
+    n[:, 1::2] = codes >> 4
+    return n - 8
+
+
+def _quantise(a):
+    """a [rows][K] -> q (int64), sigma [rows][K / 32]: 16 bits per group of 32."""
+    ag = a.reshape(a.shape[0], -1, G)
+    amax = np.abs(ag).max(axis=-1)
+    e = np.floor(np.log2(np.where(amax > 0, amax, 1.0)))
+    sigma = np.where(amax >= 2.0 ** -100, np.exp2(e - 14), 0.0)
+    inv = np.where(sigma > 0, 1.0 / np.where(sigma > 0, sigma, 1.0), 0.0)
+    q = np.clip(np.rint(ag * inv[..., None]), -32767, 32767).astype(np.int64)
+    return q, sigma
+
+
+def _gemv(a, n, s):
+    """out[t][j] = fp32 sum over groups of fp32(sum_k n q) * (s_jg sigma_tg)."""
+    q, sigma = _quantise(a)
+    ng = n.reshape(n.shape[0], -1, G)                       # [N][groups][32]
+    isum = np.einsum("tgk,jgk->tjg", q, ng)                  # exact integers
+    assert np.abs(isum).max() < 2 ** 23
+    sc = (s[None, :, :] * sigma[:, None, :]).astype(np.float32)
+    return np.sum((isum.astype(np.float32) * sc), axis=-1, dtype=np.float32).astype(np.float64)
+
+
+@pytest.fixture(scope="module")
+def expert():
+    wl = synthetic.Workload("int4_gemv_model", T, 4096, 1, 1536, 1536, 1, "int4", 2, tokens=(T,))
+    ex = {k: v[0] for k, v in synthetic.gen_experts(wl).items()}
+    xf = synthetic.bf16_bits_to_f32(synthetic.gen_x(wl, T=T)).astype(np.float64)
+    ref = np.stack([oracle.expert_ffn(xf[t], "int4", ex["gate"], ex["up"], ex["down"],
+                                      ex["gate_scale"], ex["up_scale"], ex["down_scale"])
+                    for t in range(T)])
+    W = {m: (_codes(ex[m]), synthetic.bf16_bits_to_f32(ex[m + "_scale"]).astype(np.float64))
+         for m in ("gate", "up", "down")}
+    return xf, W, ref
+
+
+def _h(xf, W):
+    g = _gemv(xf, *W["gate"]).astype(np.float32)
+    u = _gemv(xf, *W["up"]).astype(np.float32)
+    gc = np.minimum(g, np.float32(10))
+    h = gc / (np.float32(1) + np.exp(-gc)) * np.clip(u, np.float32(-10), np.float32(10))
+    return h.astype(np.float64)
+
+
+def test_bf16_x_is_exact_near_each_group_max(expert):
+    xf, _, _ = expert
+    q, sigma = _quantise(xf)
+    xq = (q * sigma[..., None]).reshape(xf.shape)
+    mx = np.repeat(np.abs(xf).reshape(T, -1, G).max(axis=-1), G, axis=1)
+    err = np.abs(xq - xf)
+    assert np.all(err[np.abs(xf) >= mx * 2.0 ** -7] == 0)
+    assert np.all(err <= mx * 2.0 ** -15)
+
+
+def test_16_bit_activations_keep_the_expert_output_inside_the_tolerance(expert):
+    xf, W, ref = expert
+    h = _h(xf, W)
+    y = _gemv(h, *W["down"])
+    err = rel_max_err(y, ref)
+    # the same h rounded to fp16 instead of 16-bit groups, for comparison
+    n, s = W["down"]
+    w_down = (n * np.repeat(s, G, axis=1)).astype(np.float64)
+    err16 = rel_max_err((h.astype(np.float16).astype(np.float64) @ w_down.T).astype(np.float32), ref)
+    assert err <= 5e-4  # measured 2.3e-4: a tenth of the 5e-3 Int4 tolerance at most
+    assert err < err16  # fp16 h: 9.5e-4
