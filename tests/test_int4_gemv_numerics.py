@@ -12,9 +12,10 @@ activations keep the expert output far inside the Int4 tolerance (5e-3 of
 RMS), tighter than fp16 h would.  Measured with this model: max err / RMS
 2.3e-4, nearly all of it h's quantisation (2.6e-4 alone; x's 2.7e-5): the
 clamped SwiGLU reaches |h| ~ 100 on this workload, and a group's small
-values share the quantum of its largest one (2^-15 of it).  The offset-binary decode, value = (nibble
-- 8) * scale, is the grouped fmt=4 format of "feat(glm53): add
-device-resident HIP backend for MI350P", "Key changes".
+values share the quantum of its largest one (2^-15 of it).  The
+offset-binary decode, value = (nibble - 8) * scale, is the grouped fmt=4
+format of "feat(glm53): add device-resident HIP backend for MI350P", "Key
+changes".
 """
 import numpy as np
 import pytest
